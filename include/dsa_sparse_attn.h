@@ -1,0 +1,128 @@
+/*
+ * dsa_sparse_attn.h -- C ABI of the fused top-k sparse latent-attention kernel for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation (stages as named on "Deepseek V41 Attention MegaKernel", vLLM PR #56344,
+ * Purpose: fused norm + RoPE + sparse attention + inverse RoPE + FP8 cast).  For every
+ * query token t and head h:
+ *   1. q~ = RMSNorm(q[t,h,:576]) * norm_w   (fp32 statistics, eps = rms_eps)
+ *   2. RoPE on q~ dims 512..575: pairs (512+2i, 513+2i) rotated by
+ *      positions[t] * rope_base^(-2i/64)
+ *   3. valid columns j: j < topk_length[t] and indices[t,j] >= 0 (the page's sentinel
+ *      fix: reads are capped at topk_length and -1 entries are never read); columns
+ *      j < n_swa_cols read kv_swa[indices[t,j]], the others kv_cmp[indices[t,j]]
+ *   4. k = dequantised 512 latent values ++ 64 rope values of the row, v = latent
+ *   5. o = softmax_j(softmax_scale * q~.k_j) weighted sum of v_j  (o = 0 when no column
+ *      is valid)
+ *   6. inverse RoPE on o dims 448..511 (angle -positions[t] * theta_i)
+ *   7. MXFP8 cast of o: per 32-value block along the 512 dims, UE8M0 scale code
+ *      E + 127 with E = floor(log2(block amax)) - 8 clamped to [-127, 127] (0 for an
+ *      all-zero block), values o / 2^E rounded to E4M3 (ties to even, saturating).
+ *
+ * Data layouts (all row-major, all pointers are DEVICE pointers owned by the caller;
+ * the library never allocates, frees or retains them):
+ *   q           bf16  [s_q, h_q, 576]                  16-byte aligned
+ *   kv_swa      uint8 [n_swa_rows, 656] fp8_ds_mla rows 16-byte aligned
+ *   kv_cmp      uint8 [n_cmp_rows, 656] fp8_ds_mla rows 16-byte aligned
+ *               row = 512 E4M3 latent | 4 little-endian fp32 scales (one per 128
+ *               latent values) | 64 bf16 rope values
+ *   indices     int32 [s_q, topk]   (-1 or any negative value = skip)
+ *   topk_length int32 [s_q]         (values <= 0 read nothing; values > topk read topk)
+ *   positions   int32 [s_q]
+ *   norm_w      bf16  [576]
+ *   out_fp8     uint8 [s_q, h_q, 512] E4M3 codes          4-byte aligned
+ *   out_sf      uint8 [s_q, h_q, 16]  UE8M0 codes
+ *   out_precast fp32  [s_q, h_q, 512] (debug entry only; may be NULL)
+ *   lse         fp32  [s_q, h_q] natural-log sum-exp of the scaled scores, -inf for
+ *               a token with no valid column (debug entry only; may be NULL)
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream),
+ * allocate nothing, and launch one kernel after one small memset of the workspace
+ * header.  Arguments are checked on the host before anything is enqueued; a non-zero
+ * return means nothing was enqueued (DSA_ERR_CUDA: the launch itself failed).
+ * An index >= its pool's row count is undefined behaviour unless
+ * DSA_FLAG_CHECK_INDICES is set; then that column is skipped and the device status
+ * word gets DSA_STATUS_INDEX_OUT_OF_RANGE (read it with dsa_sparse_attn_read_status).
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef DSA_SPARSE_ATTN_H_
+#define DSA_SPARSE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG (-1)         /* null/misaligned pointer, bad parameter */
+#define DSA_ERR_UNSUPPORTED_SHAPE (-2)   /* h_q outside [1,64], topk > DSA_MAX_TOPK, ... */
+#define DSA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define DSA_ERR_CUDA (-4)                /* CUDA runtime error (launch, attribute, memset) */
+#define DSA_ERR_UNSUPPORTED_DEVICE (-5)  /* current device is not compute capability 10.3 */
+
+#define DSA_FLAG_CHECK_INDICES 1u        /* bounds-check every index against its pool */
+
+#define DSA_STATUS_INDEX_OUT_OF_RANGE 1u /* an index was >= its pool size (with the flag) */
+#define DSA_STATUS_WAIT_TIMEOUT 2u       /* an on-chip pipeline wait gave up; output invalid */
+
+#define DSA_MAX_HEADS 64
+#define DSA_MAX_TOPK 2048
+#define DSA_ROW_BYTES 656
+
+typedef struct dsa_params {
+  int32_t s_q;          /* query tokens (>= 0) */
+  int32_t h_q;          /* query heads, 1..64, sharing one latent KV head */
+  int32_t topk;         /* index columns per token, 0..DSA_MAX_TOPK */
+  int32_t n_swa_cols;   /* columns [0, n_swa_cols) index kv_swa, [n_swa_cols, topk) kv_cmp */
+  int64_t n_swa_rows;   /* rows in kv_swa (< 2^31) */
+  int64_t n_cmp_rows;   /* rows in kv_cmp (< 2^31) */
+  float softmax_scale;  /* e.g. 1/sqrt(576) */
+  float rope_base;      /* e.g. 10000 */
+  float rms_eps;        /* e.g. 1e-6 */
+  uint32_t flags;       /* DSA_FLAG_* */
+} dsa_params;
+
+/* Fill `p` with the defaults above for the given shape (softmax_scale 1/sqrt(576),
+ * rope_base 10000, rms_eps 1e-6, flags 0).  Returns DSA_OK or DSA_ERR_INVALID_ARG. */
+int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32_t n_swa_cols,
+                    int64_t n_swa_rows, int64_t n_cmp_rows);
+
+/* Bytes of device workspace the forward call needs for `p` on a GPU with `num_sms`
+ * SMs (num_sms <= 0: the current device).  The workspace holds a status word, one
+ * combine counter per token and, when a token's rows are split across several CTAs,
+ * the per-split partial outputs.  0 is returned for invalid parameters. */
+size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
+
+/* The fused forward pass (steps 1-7). */
+int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp,
+                        const int32_t* indices, const int32_t* topk_length,
+                        const int32_t* positions, const void* norm_w,
+                        void* out_fp8, uint8_t* out_sf, const dsa_params* p,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same computation; additionally writes the pre-cast fp32 output (after inverse
+ * RoPE) and the LSE when the pointers are non-NULL. */
+int dsa_sparse_attn_fwd_debug(const void* q, const void* kv_swa, const void* kv_cmp,
+                              const int32_t* indices, const int32_t* topk_length,
+                              const int32_t* positions, const void* norm_w,
+                              void* out_fp8, uint8_t* out_sf, float* out_precast, float* lse,
+                              const dsa_params* p, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Waits for `stream`, then copies the device status word (DSA_STATUS_* bits of the
+ * last call that used `workspace`) into *status.  Returns DSA_OK or an error code. */
+int dsa_sparse_attn_read_status(const void* workspace, uint32_t* status, void* stream);
+
+/* Split count the forward call uses for a shape (exposed for tests and tooling). */
+int dsa_sparse_attn_num_splits(const dsa_params* p, int num_sms);
+
+/* Static description of an error code. */
+const char* dsa_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_SPARSE_ATTN_H_ */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads and exports every
+function the header declares; argument validation fails before anything touches a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from top_sparse_mla_gb300 import native
+from top_sparse_mla_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa_sparse_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return native.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(dsa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in native.EXPORTED:
+        assert n in names, n
+    assert set(names) == set(native.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"missing export {name}"
+
+
+def test_params_init_defaults(lib):
+    p = native.dsa_params_init(4, 64, 640, 128, 1000, 2000)
+    assert (p.s_q, p.h_q, p.topk, p.n_swa_cols, p.n_swa_rows, p.n_cmp_rows) == (4, 64, 640, 128, 1000, 2000)
+    assert abs(p.softmax_scale - 1 / 24) < 1e-8 and p.rope_base == 10000.0 and abs(p.rms_eps - 1e-6) < 1e-12
+    assert p.flags == 0
+    assert lib.dsa_params_init(None, 1, 1, 1, 1, 1, 1) == native.DSA_ERR_INVALID_ARG
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert len(native.dsa_error_string(code)) > 0
+
+
+def test_split_heuristic_and_workspace_size(lib):
+    p = native.dsa_params_init(1, 64, 640, 128, 8192, 65536)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 5          # one 128-row tile per split
+    p = native.dsa_params_init(64, 64, 640, 128, 8192, 262144)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 2
+    p = native.dsa_params_init(1024, 64, 640, 128, 131072, 1 << 20)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 1
+    ws1 = native.dsa_sparse_attn_workspace_size(p, 152)
+    assert ws1 >= 256 + 4 * 1024 and ws1 % 256 == 0
+    p = native.dsa_params_init(64, 64, 640, 128, 8192, 262144)
+    ws2 = native.dsa_sparse_attn_workspace_size(p, 152)
+    assert ws2 >= 64 * 2 * 64 * 512 * 4                              # per-split partial outputs
+    bad = native.dsa_params_init(1, 65, 640, 128, 1, 1)
+    assert native.dsa_sparse_attn_workspace_size(bad, 152) == 0
+
+
+def _call(lib, p, **over):
+    args = dict(q=16, kv_swa=16, kv_cmp=16, indices=16, topk_length=16, positions=16, norm_w=16, out_fp8=16,
+                out_sf=16, ws=256, ws_bytes=1 << 30)
+    args.update(over)
+    return lib.dsa_sparse_attn_fwd(args["q"], args["kv_swa"], args["kv_cmp"], args["indices"], args["topk_length"],
+                                   args["positions"], args["norm_w"], args["out_fp8"], args["out_sf"],
+                                   ctypes.byref(p) if p is not None else None, args["ws"], args["ws_bytes"], None)
+
+
+def test_argument_validation_happens_before_any_gpu_work(lib):
+    ok = native.dsa_params_init(2, 64, 640, 128, 1000, 2000)
+    assert _call(lib, None) == native.DSA_ERR_INVALID_ARG
+    for field in ("q", "topk_length", "positions", "norm_w", "out_fp8", "out_sf", "ws", "indices", "kv_swa", "kv_cmp"):
+        assert _call(lib, ok, **{field: None}) == native.DSA_ERR_INVALID_ARG, field
+    assert _call(lib, ok, q=8) == native.DSA_ERR_INVALID_ARG          # q not 16-byte aligned
+    assert _call(lib, ok, kv_cmp=24) == native.DSA_ERR_INVALID_ARG    # pool not 16-byte aligned
+    assert _call(lib, ok, ws=128) == native.DSA_ERR_INVALID_ARG       # workspace not 256-byte aligned
+    assert _call(lib, ok, out_fp8=2) == native.DSA_ERR_INVALID_ARG
+    for h in (0, 65):
+        p = native.dsa_params_init(2, h, 640, 128, 1000, 2000)
+        assert _call(lib, p) == native.DSA_ERR_UNSUPPORTED_SHAPE
+    p = native.dsa_params_init(2, 64, 4096, 128, 1000, 2000)
+    assert _call(lib, p) == native.DSA_ERR_UNSUPPORTED_SHAPE
+    p = native.dsa_params_init(2, 64, 640, 700, 1000, 2000)
+    assert _call(lib, p) == native.DSA_ERR_INVALID_ARG                 # n_swa_cols > topk
+    p = native.dsa_params_init(-1, 64, 640, 128, 1000, 2000)
+    assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
+    p = native.dsa_params_init(2, 64, 640, 128, 1 << 31, 2000)
+    assert _call(lib, p) == native.DSA_ERR_UNSUPPORTED_SHAPE
+    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, flags=8)
+    assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
+    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, softmax_scale=float("nan"))
+    assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    p = native.dsa_params_init(0, 64, 640, 128, 1000, 2000)
+    assert _call(lib, p) == native.DSA_OK
+    # swa-only / cmp-only shapes do not need the other pool
+    p = native.dsa_params_init(2, 64, 640, 640, 1000, 0)
+    assert _call(lib, p, kv_cmp=None, q=8) == native.DSA_ERR_INVALID_ARG   # fails on q, not on the missing pool

@@ -1,0 +1,158 @@
+"""ctypes binding of the C ABI in include/dsa_sparse_attn.h (argument marshalling only).
+
+Every entry point keeps the C name.  Tensors are passed as raw device pointers
+(``tensor.data_ptr()``); the stream is the caller's current CUDA stream.  All of the
+computation happens in the CUDA library; when the library is missing this module raises
+instead of falling back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARG = -1
+DSA_ERR_UNSUPPORTED_SHAPE = -2
+DSA_ERR_WORKSPACE_TOO_SMALL = -3
+DSA_ERR_CUDA = -4
+DSA_ERR_UNSUPPORTED_DEVICE = -5
+DSA_FLAG_CHECK_INDICES = 1
+DSA_STATUS_INDEX_OUT_OF_RANGE = 1
+DSA_STATUS_WAIT_TIMEOUT = 2
+DSA_MAX_HEADS = 64
+DSA_MAX_TOPK = 2048
+DSA_ROW_BYTES = 656
+
+EXPORTED = (
+    "dsa_params_init",
+    "dsa_sparse_attn_workspace_size",
+    "dsa_sparse_attn_fwd",
+    "dsa_sparse_attn_fwd_debug",
+    "dsa_sparse_attn_read_status",
+    "dsa_sparse_attn_num_splits",
+    "dsa_error_string",
+)
+
+
+class DsaParams(ctypes.Structure):
+    _fields_ = [
+        ("s_q", ctypes.c_int32),
+        ("h_q", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("n_swa_cols", ctypes.c_int32),
+        ("n_swa_rows", ctypes.c_int64),
+        ("n_cmp_rows", ctypes.c_int64),
+        ("softmax_scale", ctypes.c_float),
+        ("rope_base", ctypes.c_float),
+        ("rms_eps", ctypes.c_float),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {dsa_error_string(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with top_sparse_mla_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    pp = ctypes.POINTER(DsaParams)
+    lib.dsa_params_init.argtypes = [pp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int64, ctypes.c_int64]
+    lib.dsa_params_init.restype = ctypes.c_int
+    lib.dsa_sparse_attn_workspace_size.argtypes = [pp, ctypes.c_int]
+    lib.dsa_sparse_attn_workspace_size.restype = sz
+    lib.dsa_sparse_attn_num_splits.argtypes = [pp, ctypes.c_int]
+    lib.dsa_sparse_attn_num_splits.restype = ctypes.c_int
+    lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, pp, vp, sz, vp]
+    lib.dsa_sparse_attn_fwd.restype = ctypes.c_int
+    lib.dsa_sparse_attn_fwd_debug.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, pp, vp, sz, vp]
+    lib.dsa_sparse_attn_fwd_debug.restype = ctypes.c_int
+    lib.dsa_sparse_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.dsa_sparse_attn_read_status.restype = ctypes.c_int
+    lib.dsa_error_string.argtypes = [ctypes.c_int]
+    lib.dsa_error_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def dsa_error_string(code: int) -> str:
+    return library().dsa_error_string(int(code)).decode()
+
+
+def dsa_params_init(s_q, h_q, topk, n_swa_cols, n_swa_rows, n_cmp_rows, **overrides) -> DsaParams:
+    p = DsaParams()
+    rc = library().dsa_params_init(ctypes.byref(p), s_q, h_q, topk, n_swa_cols, n_swa_rows, n_cmp_rows)
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_params_init")
+    for k, v in overrides.items():
+        setattr(p, k, v)
+    return p
+
+
+def dsa_sparse_attn_workspace_size(p: DsaParams, num_sms: int = 0) -> int:
+    return int(library().dsa_sparse_attn_workspace_size(ctypes.byref(p), int(num_sms)))
+
+
+def dsa_sparse_attn_num_splits(p: DsaParams, num_sms: int = 0) -> int:
+    return int(library().dsa_sparse_attn_num_splits(ctypes.byref(p), int(num_sms)))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def dsa_sparse_attn_fwd(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_w, out_fp8, out_sf,
+                        p: DsaParams, workspace, workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = library().dsa_sparse_attn_fwd(_ptr(q), _ptr(kv_swa), _ptr(kv_cmp), _ptr(indices), _ptr(topk_length),
+                                       _ptr(positions), _ptr(norm_w), _ptr(out_fp8), _ptr(out_sf), ctypes.byref(p),
+                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_sparse_attn_fwd")
+
+
+def dsa_sparse_attn_fwd_debug(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_w, out_fp8, out_sf,
+                              out_precast, lse, p: DsaParams, workspace, workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = library().dsa_sparse_attn_fwd_debug(_ptr(q), _ptr(kv_swa), _ptr(kv_cmp), _ptr(indices), _ptr(topk_length),
+                                             _ptr(positions), _ptr(norm_w), _ptr(out_fp8), _ptr(out_sf),
+                                             _ptr(out_precast), _ptr(lse), ctypes.byref(p), _ptr(workspace),
+                                             int(workspace_bytes), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_sparse_attn_fwd_debug")
+
+
+def dsa_sparse_attn_read_status(workspace, stream=None) -> int:
+    st = ctypes.c_uint32(0)
+    rc = library().dsa_sparse_attn_read_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_sparse_attn_read_status")
+    return int(st.value)
