@@ -1,0 +1,359 @@
+"""Benchmark of the fused sparse-attention kernel (one JSON line on stdout).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+A step is one call of the whole fused path over one batch of synthetic tokens.  The
+headline workload is the 1024-token decode (h_q 64, top-k 128 + 512 with ragged
+lengths, NaN-filled stale rows); the line also carries the other workload sizes.
+Timing: W untimed warm-up steps, then K steps; L2 is flushed (a 512 MiB write) before
+every timed step, each step is timed with CUDA events on the launching stream, and
+the K-step region is bracketed by a barrier and a device synchronize.  With N > 1
+(torchrun) every rank runs its own copy of the workload on its own GPU (independent
+problems, no collective on the data path); the value is the tokens of all ranks over
+the slowest rank's time.
+
+--impl reference times the CPU oracle (float64 numpy, test infrastructure) on
+bounded samples of the same workload; only rank 0 runs it.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+HEADLINE = "decode1024"
+METRIC = "sparse-attn tokens/s and us/call, s_q=1..2123; HBM GB/s and % of roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes the path must move at least once: the valid gathered rows, q, the outputs,
+    the index row, the length and the position of every token."""
+    from top_sparse_mla_gb300 import workloads as W
+    n_valid = int(W.n_valid_rows(w).sum())
+    per_tok = w.h_q * 576 * 2 + w.h_q * 512 + w.h_q * 16 + w.topk * 4 + 8
+    return n_valid * 656 + w.s_q * per_tok
+
+
+def algorithmic_flops(w) -> int:
+    from top_sparse_mla_gb300 import workloads as W
+    return int(W.n_valid_rows(w).sum()) * (2 * w.h_q * 576 + 2 * w.h_q * 512)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling every 200 ms while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_kernel(inp, out, steps: int, warmup: int, flush, events=True):
+    """Per-step CUDA-event times (ms) of the fused call, L2 flushed before each step."""
+    import torch
+    from top_sparse_mla_gb300 import api
+    for _ in range(warmup):
+        flush.zero_()
+        api.forward(inp, out)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(st)
+        api.forward(inp, out)
+        ends[i].record(st)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_e2e(w, inp, out, steps: int, warmup: int, flush):
+    """Same call with the step's inputs copied from pinned host memory and the result
+    copied back, inside the timed span.  The KV caches and the norm weight stay resident
+    on the device (persistent state, like model weights)."""
+    import torch
+    from top_sparse_mla_gb300 import api
+    h_q = torch.from_numpy(w.q.view(np.int16)).pin_memory()
+    h_idx = torch.from_numpy(w.indices).pin_memory()
+    h_len = torch.from_numpy(w.topk_length).pin_memory()
+    h_pos = torch.from_numpy(w.positions).pin_memory()
+    h_fp8 = torch.empty(out.out_fp8.shape, dtype=torch.uint8).pin_memory()
+    h_sf = torch.empty(out.out_sf.shape, dtype=torch.uint8).pin_memory()
+    st = torch.cuda.current_stream()
+
+    def step():
+        inp.q.copy_(h_q, non_blocking=True)
+        inp.indices.copy_(h_idx, non_blocking=True)
+        inp.topk_length.copy_(h_len, non_blocking=True)
+        inp.positions.copy_(h_pos, non_blocking=True)
+        api.forward(inp, out)
+        h_fp8.copy_(out.out_fp8, non_blocking=True)
+        h_sf.copy_(out.out_sf, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        step()
+        b.record(st)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_len, h_pos))
+    d2h = sum(t.numel() * t.element_size() for t in (h_fp8, h_sf))
+    return times, h2d, d2h
+
+
+def cpu_oracle_rate(w, max_seconds: float = 20.0, min_tokens: int = 32):
+    """Oracle tokens/s on a bounded prefix of the workload's tokens."""
+    import oracle
+    p = oracle.OracleParams(n_swa_cols=w.n_swa_cols)
+    t0 = time.time()
+    done = 0
+    chunk = 16
+    while done < w.s_q and (time.time() - t0 < max_seconds or done < min_tokens):
+        sel = np.arange(done, min(done + chunk, w.s_q))
+        oracle.sparse_mla_forward(w.q[sel], w.kv_swa, w.kv_cmp, w.indices[sel], w.topk_length[sel],
+                                  w.positions[sel], w.norm_w, p)
+        done += len(sel)
+    dt = time.time() - t0
+    return done / dt, done, dt
+
+
+def run_reference(args):
+    world, rank, _, pg = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    from top_sparse_mla_gb300 import workloads as W
+    w = W.make(HEADLINE)
+    import oracle
+    p = oracle.OracleParams(n_swa_cols=w.n_swa_cols)
+    per_step = 32
+    cores = len(os.sched_getaffinity(0))
+
+    def step(i):
+        start = (i * per_step) % w.s_q
+        sel = np.arange(start, min(start + per_step, w.s_q))
+        oracle.sparse_mla_forward(w.q[sel], w.kv_swa, w.kv_cmp, w.indices[sel], w.topk_length[sel],
+                                  w.positions[sel], w.norm_w, p)
+        return len(sel)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.time()
+    toks = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.time() - t0
+    value = toks / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "s_q_per_step": per_step, "h_q": w.h_q, "topk": w.topk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{toks} tokens of {w.name} ({per_step} per step), numpy float64, BLAS default threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import torch
+    world, rank, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    from top_sparse_mla_gb300 import api, native, workloads as W
+    from top_sparse_mla_gb300.build import build
+    build()
+    native.library()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    peak, peak_kind = measured_peaks()
+
+    w = W.make(args.workload)
+    inp = api.upload(w, "cuda")
+    out = api.allocate_outputs(inp)
+    sampler = ClockSampler(local)
+    barrier(pg)
+    torch.cuda.synchronize()
+    t_wall = time.time()
+    times = time_kernel(inp, out, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(pg)
+    wall = time.time() - t_wall
+    # keep the GPU under the same load long enough for the clock sampler to see it
+    soak_end = time.time() + (0.0 if args.no_soak else 1.5)
+    while time.time() < soak_end:
+        time_kernel(inp, out, 20, 0, flush)
+    clocks = sampler.stop()
+    ms = statistics.mean(times)
+    ms_max = max_over_ranks(pg, ms)
+    tokens_total = w.s_q * world
+    value = tokens_total / (ms_max * 1e-3)
+    b_alg = algorithmic_bytes(w)
+    achieved = b_alg / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.skip_e2e:
+        e2e_times, h2d, d2h = time_e2e(w, inp, out, max(3, min(args.steps, 20)), 2, flush)
+        e2e_ms = max_over_ranks(pg, statistics.mean(e2e_times))
+        e2e = {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    per_config = {}
+    if not args.skip_sweep:
+        for name in ("decode1", "decode64", "decode1024", "prefill2123"):
+            wc = W.make(name) if name != args.workload else w
+            ic = api.upload(wc, "cuda") if name != args.workload else inp
+            oc = api.allocate_outputs(ic)
+            tc = time_kernel(ic, oc, 30, 5, flush)
+            med = statistics.median(tc)
+            bc = algorithmic_bytes(wc)
+            per_config[name] = {"us_per_call_median": med * 1e3, "us_per_call_mean": statistics.mean(tc) * 1e3,
+                                "tokens_per_s": wc.s_q / (med * 1e-3), "alg_bytes": bc,
+                                "alg_gbs": bc / (med * 1e-3) / 1e9, "frac_of_hbm_peak": bc / (med * 1e-3) / 1e9 / peak,
+                                "alg_tflops": algorithmic_flops(wc) / (med * 1e-3) / 1e12,
+                                "n_valid_rows": int(W.n_valid_rows(wc).sum())}
+            if name != args.workload:
+                del ic, oc
+                torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        rate, ntok, dt = cpu_oracle_rate(w)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"first {ntok} tokens of {w.name} in {dt:.1f} s, numpy float64, BLAS default threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": w.name, "s_q": w.s_q, "h_q": w.h_q, "topk": w.topk,
+                       "n_valid_rows": int(W.n_valid_rows(w).sum()), "parallelism": f"independent x{world}",
+                       "l2": "flushed before every timed step (512 MiB write)",
+                       "operands": "fp8 e4m3 cache dequantised to fp16, fp32 accumulate, MXFP8 out",
+                       "timed_wall_s": wall},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": args.traffic, "peak_source": peak_kind,
+                         "alg_bytes_per_launch": b_alg},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "per_config": per_config,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=HEADLINE, help="workload timed for the headline line")
+    ap.add_argument("--skip-sweep", action="store_true", help="headline workload only")
+    ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end timing")
+    ap.add_argument("--no-soak", action="store_true", help="no clock-sampling soak after the timed steps")
+    ap.add_argument("--skip-cpu", action="store_true", help="no CPU oracle baseline")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the kernel from an ncu capture, if known")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -30,9 +30,9 @@
  *   topk_length int32 [s_q]         (values <= 0 read nothing; values > topk read topk)
  *   positions   int32 [s_q]
  *   norm_w      bf16  [576]
- *   out_fp8     uint8 [s_q, h_q, 512] E4M3 codes          4-byte aligned
+ *   out_fp8     uint8 [s_q, h_q, 512] E4M3 codes          16-byte aligned
  *   out_sf      uint8 [s_q, h_q, 16]  UE8M0 codes
- *   out_precast fp32  [s_q, h_q, 512] (debug entry only; may be NULL)
+ *   out_precast fp32  [s_q, h_q, 512] (debug entry only; may be NULL) 16-byte aligned
  *   lse         fp32  [s_q, h_q] natural-log sum-exp of the scaled scores, -inf for
  *               a token with no valid column (debug entry only; may be NULL)
  *

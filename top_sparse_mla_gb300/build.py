@@ -25,7 +25,8 @@ def nvcc_path() -> str:
 
 def build(verbose: bool = False, extra_flags=None) -> str:
     """Build the shared library if any source is newer than it; return its path."""
-    deps = SOURCES + [os.path.join(INCLUDE, "dsa_sparse_attn.h"), os.path.abspath(__file__)]
+    deps = SOURCES + [os.path.join(PKG_DIR, "csrc", "ptx_sm103.cuh"), os.path.join(INCLUDE, "dsa_sparse_attn.h"),
+                      os.path.abspath(__file__)]
     if os.path.exists(LIB_PATH) and all(os.path.getmtime(LIB_PATH) >= os.path.getmtime(d) for d in deps):
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
