@@ -5,22 +5,23 @@
 //
 // Work item = (query token, KV split), taken from a global queue.  One CTA of 16 warps
 // per SM; the warps are specialised and talk through mbarriers, so consecutive items
-// overlap (the next item's index scan and q~ build run while the current item's tiles
-// are in flight):
+// and consecutive tiles overlap:
 //
-//   PREP  (warps 13-15) take an item; compact its valid index columns into a row list;
+//   PREP  (warps 13-14) take an item; compact its valid index columns into a row list;
 //                       rotary table; L2 prefetch of the rows; build q~ = RoPE(RMSNorm(q)
 //                       * w) in fp16 as the B operand of QK^T (K-major, 128-byte swizzle)
 //   KD    (warps 4-7)   one gathered row per thread -> fp16 K~ (fp32 scale folded) into a
 //                       TMEM ring: the A operand of QK^T, lane = row
 //   VD    (warps 0-3)   one gathered row per thread -> fp16 V~ into an SMEM ring in
 //                       MN-major layout: the A operand of PV
-//   MMA   (warp 12)     S^T[128 rows x 64 heads]  = K~ . q~^T     (tcgen05, M=128 N=64)
-//                       O^T[512 dims x 64 heads] += V~^T . P^T    (tcgen05, M=128 N=64)
+//   QK    (warp 12)     S^T[128 rows x 64 heads]  = K~ . q~^T     (tcgen05, M=128 N=64)
+//   PV    (warp 15)     O^T[512 dims x 64 heads] += V~^T . P^T    (tcgen05, M=128 N=64)
 //   SM    (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P), O rescale,
 //                       then the epilogue: O / l, inverse RoPE, MXFP8 cast and stores, or
 //                       the split partials and the last split's combine
 //
+// The two MMA issuers are separate threads so that QK^T of the next tile never waits
+// behind PV of the previous one.  S^T and P are double-buffered.
 // TMEM: O^T columns 0..255, S^T double buffer 256..383, K~ ring 384..511.
 // Every mbarrier wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT,
 // every role leaves its loop, the tensor core is drained and TMEM freed.
@@ -41,10 +42,10 @@ constexpr int ROW_BYTES = 656;
 constexpr int TILE = 128;           // gathered rows per tile (the M of QK^T)
 constexpr int HP = 64;              // heads as seen by the MMAs (padded)
 constexpr int NTHREADS = 512;
-constexpr int W_VD = 0, W_KD = 4, W_SM = 8, W_MMA = 12, W_PREP = 13, N_PREP_WARPS = 3;
+constexpr int W_VD = 0, W_KD = 4, W_SM = 8, W_QK = 12, W_PREP = 13, N_PREP_WARPS = 2, W_PV = 15;
 constexpr int N_PREP = 32 * N_PREP_WARPS;
 constexpr int K_SLOTS = 4;          // TMEM ring of 32-column slots (64 dims of K~ each)
-constexpr int V_SLOTS = 2;          // SMEM ring of [128 dims x 128 rows] fp16 blocks
+constexpr int V_SLOTS = 3;          // SMEM ring of [128 dims x 128 rows] fp16 blocks
 constexpr int HC_PER_TILE = 9;      // 8 latent half-chunks (64 dims) + the rope chunk
 constexpr int MAX_SPLITS = 16;
 
@@ -55,14 +56,12 @@ constexpr uint32_t TM_K = 384;      // + 32 * slot
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t EPI_STRIDE = 36;                          // floats per head row in a slab
-constexpr uint32_t EPI_WARP_BYTES = HP * EPI_STRIDE * 4;     // [64 heads x 32 dims] (+pad)
 constexpr uint32_t SM_Q = 0;                                 // q~: 9 K-atoms x 8 KB
-constexpr uint32_t SM_V = SM_Q + 9 * 8192;                   // V~ ring: 2 x 32 KB
-constexpr uint32_t SM_P = SM_V + V_SLOTS * 32768;            // P: 16 KB
-constexpr uint32_t SM_EPI = SM_P + 16384;                    // 4 warps x epilogue slab
-constexpr uint32_t SM_LIST = SM_EPI + 4 * EPI_WARP_BYTES;    // 2 x compacted row list
-constexpr uint32_t SM_ROPE = SM_LIST + 2 * DSA_MAX_TOPK * 4; // 2 x 32 x (cos, sin)
+constexpr uint32_t SM_V = SM_Q + 9 * 8192;                   // V~ ring: 3 x 32 KB
+constexpr uint32_t SM_P = SM_V + V_SLOTS * 32768;            // P: 2 x 16 KB; epilogue slabs
+constexpr uint32_t SM_KDBUF = SM_P + 2 * 16384;              // 4 KD warps x [32 rows x 128 B]
+constexpr uint32_t SM_VDSC = SM_KDBUF + 4 * 4096;            // 4 VD warps x [32 rows x 4 scales]
+constexpr uint32_t SM_ROPE = SM_VDSC + 4 * 512;              // 2 x 32 x (cos, sin)
 constexpr uint32_t SM_ITEM = SM_ROPE + 2 * 32 * 8;           // 2 x item info (8 ints)
 constexpr uint32_t SM_NORMW = SM_ITEM + 2 * 32;              // 576 fp32
 constexpr uint32_t SM_MREF = SM_NORMW + D_QK * 4;            // 64 fp32 running max (log2 units)
@@ -70,19 +69,25 @@ constexpr uint32_t SM_LACC = SM_MREF + 256;                  // 64 fp32 running 
 constexpr uint32_t SM_ALPHA = SM_LACC + 256;                 // 64 fp32 rescale / 1/l
 constexpr uint32_t SM_RED = SM_ALPHA + 256;                  // 4 warps x 64 fp32
 constexpr uint32_t SM_LPART = SM_RED + 1024;                 // 2 x 4 warps x 64 fp32 row sums
-constexpr uint32_t SM_CW = SM_LPART + 2048;                  // combine weights MAX_SPLITS x 64
-constexpr uint32_t SM_FLAG = SM_CW + MAX_SPLITS * 256;       // 2 x 4 fp32
+constexpr uint32_t SM_FLAG = SM_LPART + 2048;                // 2 x 4 fp32
 constexpr uint32_t SM_MISC = SM_FLAG + 32;                   // misc ints
 constexpr uint32_t SM_BAR = SM_MISC + 64;                    // mbarriers
-constexpr uint32_t SM_END = SM_BAR + 40 * 8;
+constexpr uint32_t SM_END = SM_BAR + 48 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;               // + alignment slack
+// the epilogue reuses the two P buffers: one [64 heads x 32 dims] fp32 slab per SM warp
+// (rows of 128 bytes, 16-byte chunks XOR-swizzled by row), the combine weights after it
+constexpr uint32_t EPI_SLAB_BYTES = HP * 32 * 4;
+constexpr uint32_t SM_CW = SM_P;                             // MAX_SPLITS x 64 fp32 (combine)
+static_assert(4 * EPI_SLAB_BYTES <= 2 * 16384, "epilogue slabs fit in the P buffers");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 enum {
   B_KFULL = 0, B_KEMPTY = B_KFULL + K_SLOTS, B_VFULL = B_KEMPTY + K_SLOTS, B_VEMPTY = B_VFULL + V_SLOTS,
-  B_SFULL = B_VEMPTY + V_SLOTS, B_SEMPTY = B_SFULL + 2, B_ITFULL = B_SEMPTY + 2, B_ITEMPTY = B_ITFULL + 2,
-  B_PFULL = B_ITEMPTY + 2, B_PEMPTY, B_ODONE, B_OFREE, B_QREADY, B_QFREE, B_GRP, B_PREP, B_DRAIN, B_COUNT
+  B_SFULL = B_VEMPTY + V_SLOTS, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2,
+  B_ITFULL = B_PEMPTY + 2, B_ITEMPTY = B_ITFULL + 2,
+  B_ODONE = B_ITEMPTY + 2, B_OFREE, B_QREADY, B_QFREE, B_GRP, B_PREP, B_DRAIN, B_COUNT
 };
-static_assert(B_COUNT <= 40, "barrier area");
+static_assert(B_COUNT <= 48, "barrier area");
 
 enum { M_TMEM = 0, M_ABORT, M_LAST };                           // misc ints
 enum { IT_ITEM = 0, IT_TOKEN, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS }; // item info ints
@@ -104,6 +109,7 @@ struct KParams {
   uint32_t* counters;   // [s_q] split arrivals
   uint32_t* status;
   uint32_t* work;       // global item queue head
+  uint32_t* lists;      // [grid][2][DSA_MAX_TOPK] compacted row lists (bit 31: compressed pool)
   int s_q, h_q, topk, n_swa_cols;
   long long n_swa_rows, n_cmp_rows;
   float score_scale_log2;   // softmax_scale * log2(e)
@@ -160,7 +166,8 @@ DSA_DEV const uint8_t* row_ptr(const KParams& P, uint32_t e) {
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
   const int pt = pw * 32 + lane;
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
-  const float* s_normw = reinterpret_cast<const float*>(c.sm + SM_NORMW);
+  // volatile: re-read per head group instead of 72 weights held in registers
+  const volatile float* s_normw = reinterpret_cast<const volatile float*>(c.sm + SM_NORMW);
   uint32_t n_prep_sync = 0;
   auto prep_sync = [&]() -> bool {
     mbar_arrive(bar(c, B_PREP));
@@ -186,7 +193,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
     const int split = item % P.n_splits;
     if (pw == 0) {
       // compact the valid columns (j < topk_length, index >= 0), 256 indices per load batch
-      uint32_t* list = reinterpret_cast<uint32_t*>(c.sm + SM_LIST) + DSA_MAX_TOPK * b;
+      uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
       int L = P.topk_length[t];
       L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
       const int32_t* irow = P.indices + (size_t)t * P.topk;
@@ -232,7 +239,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
         info[IT_ROW0] = row0;
         info[IT_NROWS] = nrows;
       }
-    } else if (pw == 1) {
+    } else {
       // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
       float2* rope = reinterpret_cast<float2*>(c.sm + SM_ROPE) + 32 * b;
       const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[lane];
@@ -240,39 +247,33 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
       float sn, cs;
       sincospif(2.0f * frac, &sn, &cs);
       rope[lane] = make_float2(cs, sn);
-    } else {
       if (lane == 0) prefetch_l2(P.q + (size_t)t * P.h_q * D_QK, (uint32_t)(P.h_q * D_QK * 2));
     }
     if (!prep_sync()) return;
     mbar_arrive(bar(c, B_ITFULL + b));   // rows, table and tile range published
 
-    // q~ for this item, once the previous item's QK^T no longer reads the buffer
+    // q~ for this item, once the previous item's QK^T no longer reads the buffer.
+    // Eight lanes per head, four heads per warp at a time, the next four heads' loads
+    // in flight while the current ones are normalised and stored.
     if (!wait_bar_w(c, B_QFREE, (seq & 1) ^ 1)) return;
     if (info[IT_T] > 0) {
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
       const float eps = P.rms_eps;
-      uint4 raw[2][3];
-      auto load_head = [&](int h, uint4 (&dst)[3]) {
+      const int sub = lane >> 3, sl = lane & 7;     // head slot within the group, lane within the head
+      uint4 raw[2][9];
+      auto load_group = [&](int h0, uint4 (&dst)[9]) {
+        const int h = h0 + sub;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int ch = lane + 32 * k;
-          dst[k] = (h < P.h_q && ch < 72) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + ch * 8)
-                                          : make_uint4(0, 0, 0, 0);
-        }
+        for (int k = 0; k < 9; ++k)
+          dst[k] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + (sl + 8 * k) * 8)
+                               : make_uint4(0, 0, 0, 0);
       };
-      load_head(pw, raw[0]);
-#pragma unroll 1
-      for (int i = 0, h = pw; h < HP; ++i, h += N_PREP_WARPS) {
-        uint4 cur[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) cur[k] = (i & 1) ? raw[1][k] : raw[0][k];
-        if (h + N_PREP_WARPS < HP) {
-          if (i & 1) load_head(h + N_PREP_WARPS, raw[0]);
-          else load_head(h + N_PREP_WARPS, raw[1]);
-        }
+      // warp pw builds heads [32 pw, 32 pw + 32), four at a time
+      auto process = [&](const uint4 (&cur)[9], int it) {
+        const int h = 32 * pw + 4 * it + sub;
         float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
+        for (int k = 0; k < 9; ++k) {
           const uint32_t w4[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -280,14 +281,14 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
             ss = fmaf(a, a, fmaf(bb, bb, ss));
           }
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
         const float inv = rsqrtf(ss * (1.0f / D_QK) + eps);
         const bool live = h < P.h_q;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int ch = lane + 32 * k;
-          if (ch >= 72) continue;
+        for (int k = 0; k < 9; ++k) {
+          const int ch = sl + 8 * k;           // 16-byte chunk of the head row (8 dims)
           const uint32_t w4[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
           float x[8];
 #pragma unroll
@@ -295,7 +296,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
             x[2 * e] = __uint_as_float(w4[e] << 16) * inv * s_normw[ch * 8 + 2 * e];
             x[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u) * inv * s_normw[ch * 8 + 2 * e + 1];
           }
-          if (ch >= 64) {
+          if (k == 8) {                         // chunks 64..71: the rotary dims 512..575
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 r = rope[(ch - 64) * 4 + e];
@@ -313,6 +314,14 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
           const uint32_t atom = ch >> 3, cc = ch & 7;
           sts128(c.sb + SM_Q + atom * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((cc ^ (h & 7)) << 4), o);
         }
+      };
+      load_group(32 * pw, raw[0]);
+#pragma unroll 1
+      for (int it = 0; it < 8; it += 2) {
+        load_group(32 * pw + 4 * (it + 1), raw[1]);
+        process(raw[0], it);
+        if (it + 2 < 8) load_group(32 * pw + 4 * (it + 2), raw[0]);
+        process(raw[1], it + 1);
       }
       fence_async_smem();
     }
@@ -320,43 +329,11 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
   }
 }
 
-// ================================================================== MMA
-struct PvTile {
-  bool valid, first, last;
-};
-
-DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
+// ================================================================== QK issuer
+DSA_DEV void qk_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   constexpr uint32_t IDESC_QK = idesc_f16(128, HP, 0, 0);
-  constexpr uint32_t IDESC_PV = idesc_f16(128, HP, 1, 1);
   const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  uint32_t kq = 0, vq = 0, g = 0, gpv = 0, n_ot = 0;
-  PvTile prev = {false, false, false};
-  auto pv = [&](const PvTile& x) -> bool {
-    if (x.first) {
-      if (n_ot > 0 && !wait_bar(c, B_OFREE, (n_ot - 1) & 1)) return false;
-      ++n_ot;
-    }
-    if (!wait_bar(c, B_PFULL, gpv & 1)) return false;
-    tc_fence_after();
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t slot = vq % V_SLOTS;
-      if (!wait_bar(c, B_VFULL + slot, (vq / V_SLOTS) & 1)) return false;
-      tc_fence_after();
-      const uint32_t vbase = c.sb + SM_V + slot * 32768;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sdesc(vbase + kk * 2048, 16384, 1024);
-        const uint64_t bd = sdesc(c.sb + SM_P + kk * 2048, 16384, 1024);
-        mma_ss(tmem + TM_O + 64 * j, ad, bd, IDESC_PV, (x.first && kk == 0) ? 0u : 1u);
-      }
-      tc_commit(bar(c, B_VEMPTY + slot));
-      ++vq;
-    }
-    tc_commit(bar(c, B_PEMPTY));
-    if (x.last) tc_commit(bar(c, B_ODONE));
-    ++gpv;
-    return true;
-  };
+  uint32_t kq = 0, g = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
     const int* info = s_items + 8 * b;
@@ -364,12 +341,7 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
     const int item = info[IT_ITEM];
     const int T = info[IT_T];
     mbar_arrive(bar(c, B_ITEMPTY + b));
-    if (item < 0) break;
-    // the previous item's last PV first, so its epilogue does not wait for this q~
-    if (prev.valid && prev.last) {
-      if (!pv(prev)) return;
-      prev.valid = false;
-    }
+    if (item < 0) return;
     if (!wait_bar(c, B_QREADY, seq & 1)) return;
     tc_fence_after();
     for (int tt = 0; tt < T; ++tt) {
@@ -389,21 +361,65 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
         ++kq;
       }
       tc_commit(bar(c, B_SFULL + sb));
-      if (tt == T - 1) tc_commit(bar(c, B_QFREE));
-      if (prev.valid && !pv(prev)) return;
-      prev = {true, tt == 0, tt == T - 1};
       ++g;
     }
-    if (T == 0) tc_commit(bar(c, B_QFREE));
+    tc_commit(bar(c, B_QFREE));   // once per item: q~ may be rebuilt after these MMAs
   }
-  if (prev.valid) pv(prev);
+}
+
+// ================================================================== PV issuer
+DSA_DEV void pv_role(const KParams& P, const Ctx& c, uint32_t tmem) {
+  constexpr uint32_t IDESC_PV = idesc_f16(128, HP, 1, 1);
+  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
+  uint32_t vq = 0, g = 0, n_ot = 0;
+  for (uint32_t seq = 0;; ++seq) {
+    const int b = seq & 1;
+    const int* info = s_items + 8 * b;
+    if (!wait_bar(c, B_ITFULL + b, (seq >> 1) & 1)) return;
+    const int item = info[IT_ITEM];
+    const int T = info[IT_T];
+    mbar_arrive(bar(c, B_ITEMPTY + b));
+    if (item < 0) return;
+    for (int tt = 0; tt < T; ++tt) {
+      if (tt == 0) {
+        // the previous item's epilogue must have read O^T before it is overwritten
+        if (n_ot > 0 && !wait_bar(c, B_OFREE, (n_ot - 1) & 1)) return;
+        ++n_ot;
+      }
+      const uint32_t pb = g & 1;
+      if (!wait_bar(c, B_PFULL + pb, (g >> 1) & 1)) return;
+      tc_fence_after();
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t slot = vq % V_SLOTS;
+        if (!wait_bar(c, B_VFULL + slot, (vq / V_SLOTS) & 1)) return;
+        tc_fence_after();
+        const uint32_t vbase = c.sb + SM_V + slot * 32768;
+        const uint32_t pbase = c.sb + SM_P + pb * 16384;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc(vbase + kk * 2048, 16384, 1024);
+          const uint64_t bd = sdesc(pbase + kk * 2048, 16384, 1024);
+          mma_ss(tmem + TM_O + 64 * j, ad, bd, IDESC_PV, (tt == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(bar(c, B_VEMPTY + slot));
+        ++vq;
+      }
+      tc_commit(bar(c, B_PEMPTY + pb));
+      if (tt == T - 1) tc_commit(bar(c, B_ODONE));
+      ++g;
+    }
+  }
 }
 
 // ================================================================== KD
+// Rows reach the SM with coalesced loads (eight lanes read 128 contiguous bytes of a
+// row), pass through a per-warp shared-memory transpose (16-byte chunks XOR-swizzled by
+// row) and leave one row per thread, which is what a 32x32b TMEM store needs.
 DSA_DEV void kd_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
-  const int r = q4 * 32 + lane;
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
   const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
+  const uint32_t xb = c.sb + SM_KDBUF + q4 * 4096;       // this warp's transpose buffer
+  const int sub = lane >> 3, ch = lane & 7;             // loader view: row 4k + sub, chunk ch
   uint32_t kq = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
@@ -411,59 +427,85 @@ DSA_DEV void kd_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
     if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
     if (info[IT_ITEM] < 0) return;
     const int T = info[IT_T], row0 = info[IT_ROW0], nrows = info[IT_NROWS];
-    const uint32_t* list = reinterpret_cast<const uint32_t*>(c.sm + SM_LIST) + DSA_MAX_TOPK * b;
+    const uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
     for (int tt = 0; tt < T; ++tt) {
-      const int gr = tt * TILE + r;
-      const bool valid = gr < nrows;
-      const uint8_t* rp = valid ? row_ptr(P, list[row0 + gr]) : nullptr;
+      const int r = q4 * 32 + lane;                     // this thread's row (TMEM lane)
+      const bool valid = tt * TILE + r < nrows;
+      const uint32_t entry = valid ? __ldg(list + row0 + tt * TILE + r) : 0u;
+      const uint8_t* my = row_ptr(P, entry);
       __half2 s2[4];
       {
-        const uint4 sc = valid ? ldg_nc(rp + D_LAT) : make_uint4(0, 0, 0, 0);
+        const uint4 sc = valid ? ldg_nc(my + D_LAT) : make_uint4(0, 0, 0, 0);
         s2[0] = __float2half2_rn(__uint_as_float(sc.x));
         s2[1] = __float2half2_rn(__uint_as_float(sc.y));
         s2[2] = __float2half2_rn(__uint_as_float(sc.z));
         s2[3] = __float2half2_rn(__uint_as_float(sc.w));
       }
-      // two 64-byte load buffers refilled two half-chunks ahead; the rope chunk
-      // (128 bytes of bf16) arrives in both
-      uint4 buf[2][4];
+      // the eight rows this lane loads from
+      const uint8_t* src[8];
+      bool sv[8];
 #pragma unroll
-      for (int p = 0; p < 2; ++p)
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t e = __shfl_sync(0xFFFFFFFFu, entry, 4 * k + sub);
+        sv[k] = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, 4 * k + sub) != 0;
+        src[k] = row_ptr(P, e) + 16 * ch;
+      }
+      // five 128-byte batches per row: latent 0..3, then the rope bytes 528..655
+      auto load_batch = [&](int bt, uint4 (&L)[8]) {
+        const int off = bt < 4 ? 128 * bt : 528;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) buf[p][i] = valid ? ldg_nc(rp + 64 * p + 16 * i) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < 8; ++k) L[k] = sv[k] ? ldg_nc(src[k] + off) : make_uint4(0, 0, 0, 0);
+      };
+      uint4 L[8];
+      load_batch(0, L);
 #pragma unroll
-      for (int hc = 0; hc < HC_PER_TILE; ++hc) {
-        uint32_t v[32];
-        if (hc < 8) {
+      for (int bt = 0; bt < 5; ++bt) {
+        // stage the batch: row (4k + sub) chunk ch -> swizzled slot
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dequant16(buf[hc & 1][i], s2[hc >> 1], v + 8 * i);
-        } else {
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t row = 4 * k + sub;
+          sts128(xb + row * 128 + (((uint32_t)ch ^ (row & 7)) << 4), L[k]);
+        }
+        __syncwarp();
+        if (bt < 4) load_batch(bt + 1, L);                // next batch in flight
+        const int nhalf = bt < 4 ? 2 : 1;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 w = buf[i >> 2][i & 3];
-            v[4 * i + 0] = bf16x2_to_f16x2(w.x);
-            v[4 * i + 1] = bf16x2_to_f16x2(w.y);
-            v[4 * i + 2] = bf16x2_to_f16x2(w.z);
-            v[4 * i + 3] = bf16x2_to_f16x2(w.w);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (hf >= nhalf) break;
+          uint32_t v[32];
+          if (bt < 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              const uint32_t chunk = (uint32_t)(4 * hf + i);
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                           : "r"(xb + (uint32_t)lane * 128 + ((chunk ^ ((uint32_t)lane & 7)) << 4)));
+              dequant16(w, s2[bt], v + 8 * i);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint4 w;
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                           : "r"(xb + (uint32_t)lane * 128 + (((uint32_t)i ^ ((uint32_t)lane & 7)) << 4)));
+              v[4 * i + 0] = bf16x2_to_f16x2(w.x);
+              v[4 * i + 1] = bf16x2_to_f16x2(w.y);
+              v[4 * i + 2] = bf16x2_to_f16x2(w.z);
+              v[4 * i + 3] = bf16x2_to_f16x2(w.w);
+            }
           }
+          const uint32_t slot = kq % K_SLOTS;
+          if (!wait_bar_w(c, B_KEMPTY + slot, ((kq / K_SLOTS) & 1) ^ 1)) return;
+          tc_fence_after();
+          tmem_st32(tmem + tlane + TM_K + 32 * slot, v);
+          tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(c, B_KFULL + slot));
+          ++kq;
         }
-        const int nh = hc + 2;
-        if (nh < 8) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) buf[hc & 1][i] = valid ? ldg_nc(rp + 64 * nh + 16 * i) : make_uint4(0, 0, 0, 0);
-        } else if (nh < 10) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            buf[hc & 1][i] = valid ? ldg_nc(rp + 528 + 64 * (nh - 8) + 16 * i) : make_uint4(0, 0, 0, 0);
-        }
-        const uint32_t slot = kq % K_SLOTS;
-        if (!wait_bar_w(c, B_KEMPTY + slot, ((kq / K_SLOTS) & 1) ^ 1)) return;
-        tc_fence_after();
-        tmem_st32(tmem + tlane + TM_K + 32 * slot, v);
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(c, B_KFULL + slot));
-        ++kq;
+        __syncwarp();                                   // buffer free for the next batch
       }
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
@@ -471,11 +513,12 @@ DSA_DEV void kd_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
 }
 
 // ================================================================== VD
+// Eight lanes per row read 128 contiguous bytes (one d-tile of the latent) and write the
+// fp16 values straight into the MN-major V~ block; no thread-per-row mapping is needed.
 DSA_DEV void vd_role(const KParams& P, const Ctx& c, int w, int lane) {
-  const int r = w * 32 + lane;
-  const uint32_t rsw = (uint32_t)(r & 7);
-  const uint32_t roff = (uint32_t)(r >> 3) * 1024 + rsw * 128;
   const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
+  float* s_sc = reinterpret_cast<float*>(c.sm + SM_VDSC + w * 512);   // [32 rows][4 scales]
+  const int sub = lane >> 3, ch = lane & 7;
   uint32_t vq = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
@@ -483,35 +526,49 @@ DSA_DEV void vd_role(const KParams& P, const Ctx& c, int w, int lane) {
     if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
     if (info[IT_ITEM] < 0) return;
     const int T = info[IT_T], row0 = info[IT_ROW0], nrows = info[IT_NROWS];
-    const uint32_t* list = reinterpret_cast<const uint32_t*>(c.sm + SM_LIST) + DSA_MAX_TOPK * b;
+    const uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
     for (int tt = 0; tt < T; ++tt) {
-      const int gr = tt * TILE + r;
-      const bool valid = gr < nrows;
-      const uint8_t* rp = valid ? row_ptr(P, list[row0 + gr]) : nullptr;
-      const uint4 sc = valid ? ldg_nc(rp + D_LAT) : make_uint4(0, 0, 0, 0);
-      const __half2 s2[4] = {__float2half2_rn(__uint_as_float(sc.x)), __float2half2_rn(__uint_as_float(sc.y)),
-                             __float2half2_rn(__uint_as_float(sc.z)), __float2half2_rn(__uint_as_float(sc.w))};
-      uint4 buf[2][8];
+      const int r = w * 32 + lane;
+      const bool valid = tt * TILE + r < nrows;
+      const uint32_t entry = valid ? __ldg(list + row0 + tt * TILE + r) : 0u;
+      {
+        const uint4 sc = valid ? ldg_nc(row_ptr(P, entry) + D_LAT) : make_uint4(0, 0, 0, 0);
+        __syncwarp();                                   // previous tile's scales consumed
+        *reinterpret_cast<uint4*>(s_sc + 4 * lane) = sc;
+        __syncwarp();
+      }
+      const uint8_t* src[8];
+      bool sv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) buf[0][i] = valid ? ldg_nc(rp + 16 * i) : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t e = __shfl_sync(0xFFFFFFFFu, entry, 4 * k + sub);
+        sv[k] = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, 4 * k + sub) != 0;
+        src[k] = row_ptr(P, e) + 16 * ch;
+      }
+      uint4 L[2][8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) L[0][k] = sv[k] ? ldg_nc(src[k]) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (j < 3) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            buf[(j + 1) & 1][i] = valid ? ldg_nc(rp + 128 * (j + 1) + 16 * i) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 8; ++k) L[(j + 1) & 1][k] = sv[k] ? ldg_nc(src[k] + 128 * (j + 1)) : make_uint4(0, 0, 0, 0);
         }
         const uint32_t slot = vq % V_SLOTS;
         if (!wait_bar_w(c, B_VEMPTY + slot, ((vq / V_SLOTS) & 1) ^ 1)) return;
-        const uint32_t base = c.sb + SM_V + slot * 32768 + roff;
+        const uint32_t base = c.sb + SM_V + slot * 32768 + (uint32_t)(ch >> 2) * 16384;
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          uint32_t v[32];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dequant16(buf[j & 1][4 * a + i], s2[j], v + 8 * i);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            sts128(base + a * 16384 + ((cc ^ rsw) << 4), make_uint4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]));
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t row = (uint32_t)(w * 32 + 4 * k + sub);
+          const __half2 s2 = __float2half2_rn(s_sc[4 * (4 * k + sub) + j]);
+          uint32_t v[8];
+          dequant16(L[j & 1][k], s2, v);
+          // dims [16 ch, 16 ch + 16) of the d-tile = 8-dim chunks 2(ch % 4), +1 of atom ch / 4
+          const uint32_t rsw = row & 7;
+          const uint32_t rb = base + (row >> 3) * 1024 + rsw * 128;
+          const uint32_t c0 = (uint32_t)(2 * (ch & 3));
+          sts128(rb + ((c0 ^ rsw) << 4), make_uint4(v[0], v[1], v[2], v[3]));
+          sts128(rb + (((c0 + 1) ^ rsw) << 4), make_uint4(v[4], v[5], v[6], v[7]));
         }
         fence_async_smem();
         mbar_arrive(bar(c, B_VFULL + slot));
@@ -571,7 +628,10 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   float* s_lpart = reinterpret_cast<float*>(c.sm + SM_LPART);
   float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);
   float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
-  float* slab = reinterpret_cast<float*>(c.sm + SM_EPI + q4 * EPI_WARP_BYTES);
+  // this warp's epilogue slab: 64 rows (heads) of 32 fp32 (dims), 16-byte chunks of a row
+  // XOR-swizzled by (row & 7) so that both the column writes and the row reads are free
+  // of bank conflicts
+  uint8_t* slab = c.sm + SM_P + q4 * EPI_SLAB_BYTES;
   const float c2 = P.score_scale_log2;
   const float ln2 = 0.69314718055994531f;
   uint32_t g = 0, n_grp = 0, n_ot = 0;
@@ -652,11 +712,11 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         }
         if (!grp_sync()) return;
       }
-      // the previous PV must be complete before P is overwritten or O rescaled
-      if (!wait_bar_w(c, B_PEMPTY, (g & 1) ^ 1)) return;
-      tc_fence_after();
+      // P buffer g & 1 is free once the PV two tiles back has completed
+      const uint32_t pb = g & 1;
+      if (!wait_bar_w(c, B_PEMPTY + pb, ((g >> 1) & 1) ^ 1)) return;
       // pass 2: P = exp2(x - m) in fp16, row r of the MN-major B operand; row sums
-      const uint32_t prow = c.sb + SM_P + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+      const uint32_t prow = c.sb + SM_P + pb * 16384 + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t a[32];
@@ -690,6 +750,9 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       tc_fence_before();
       mbar_arrive(bar(c, B_SEMPTY + sb));     // S^T fully read
       if (need && tt > 0) {
+        // O^T is rescaled once the PV of the previous tile has completed
+        if (!wait_bar_w(c, B_PEMPTY + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+        tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j < 8; ++j) {
           uint32_t a[32];
@@ -705,7 +768,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       }
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(c, B_PFULL));
+      mbar_arrive(bar(c, B_PFULL + pb));
       ++g;
     }
 
@@ -714,7 +777,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       if (!wait_bar_w(c, B_ODONE, n_ot & 1)) return;
       tc_fence_after();
     }
-    if (!grp_sync()) return;                 // last row sums written
+    if (!grp_sync()) return;                 // last row sums written, P buffers idle
     if (T > 0) fold_lpart(g - 1);
     const bool is_split = P.n_splits > 1;
     if (r < 64) {
@@ -739,7 +802,9 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int h = 32 * half + i;
-          slab[h * EPI_STRIDE + lane] = (T > 0) ? __uint_as_float(a[i]) * s_alpha[h] : 0.f;
+          const float v = (T > 0) ? __uint_as_float(a[i]) * s_alpha[h] : 0.f;
+          const uint32_t off = (uint32_t)h * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(h & 7)) << 4) + (lane & 3) * 4;
+          *reinterpret_cast<float*>(slab + off) = v;
         }
       }
       __syncwarp();
@@ -747,10 +812,9 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       for (int e = 0; e < 2; ++e) {
         const int h = lane + 32 * e;
         float v[32];
-        const float4* src = reinterpret_cast<const float4*>(slab + h * EPI_STRIDE);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float4 f = src[k];
+          const float4 f = *reinterpret_cast<const float4*>(slab + h * 128 + ((k ^ (h & 7)) << 4));
           v[4 * k] = f.x;
           v[4 * k + 1] = f.y;
           v[4 * k + 2] = f.z;
@@ -827,6 +891,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
           }
         }
       }
+      if (!grp_sync()) return;               // combine weights no longer needed
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
   }
@@ -857,22 +922,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(c, B_SFULL + i), 1);
       mbar_init(bar(c, B_SEMPTY + i), 128);
+      mbar_init(bar(c, B_PFULL + i), 128);
+      mbar_init(bar(c, B_PEMPTY + i), 1);
       mbar_init(bar(c, B_ITFULL + i), N_PREP);
-      mbar_init(bar(c, B_ITEMPTY + i), 128 + 128 + 128 + 1);   // KD, VD, SM, MMA
+      mbar_init(bar(c, B_ITEMPTY + i), 128 + 128 + 128 + 1 + 1);   // KD, VD, SM, QK, PV
     }
-    mbar_init(bar(c, B_PFULL), 128);
-    mbar_init(bar(c, B_PEMPTY), 1);
     mbar_init(bar(c, B_ODONE), 1);
     mbar_init(bar(c, B_OFREE), 128);
     mbar_init(bar(c, B_QREADY), N_PREP);
     mbar_init(bar(c, B_QFREE), 1);
     mbar_init(bar(c, B_GRP), 128);
     mbar_init(bar(c, B_PREP), N_PREP);
-    mbar_init(bar(c, B_DRAIN), 1);
+    mbar_init(bar(c, B_DRAIN), 2);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
   }
-  if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
+  if (warp == W_QK) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
   float* s_normw = reinterpret_cast<float*>(c.sm + SM_NORMW);
   for (int i = tid; i < D_QK; i += NTHREADS) s_normw[i] = __uint_as_float((uint32_t)P.norm_w[i] << 16);
   tc_fence_before();
@@ -880,10 +945,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = (uint32_t)c.misc[M_TMEM];
 
-  if (warp >= W_PREP) {
+  if (warp == W_PV) {
+    if (lane == 0) pv_role(P, c, tmem);
+  } else if (warp >= W_PREP) {
     prep_role(P, c, warp - W_PREP, lane);
-  } else if (warp == W_MMA) {
-    if (lane == 0) mma_role(P, c, tmem);
+  } else if (warp == W_QK) {
+    if (lane == 0) qk_role(P, c, tmem);
   } else if (warp >= W_SM) {
     sm_role(P, c, tmem, warp - W_SM, lane);
   } else if (warp >= W_KD) {
@@ -894,15 +961,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == W_MMA) {
-    if (lane == 0) {
-      // every MMA this CTA issued has completed before TMEM is released
-      tc_commit(bar(c, B_DRAIN));
-      const unsigned long long start = clock64();
-      while (!mbar_try(bar(c, B_DRAIN), 0) && clock64() - start < WAIT_LIMIT_CYCLES) {
-      }
+  if ((warp == W_QK || warp == W_PV) && lane == 0) {
+    // every MMA this CTA issued has completed before TMEM is released
+    tc_commit(bar(c, B_DRAIN));
+    const unsigned long long start = clock64();
+    while (!mbar_try(bar(c, B_DRAIN), 0) && clock64() - start < WAIT_LIMIT_CYCLES) {
     }
-    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == W_QK) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
@@ -910,7 +978,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
 
 // ================================================================== host side
 struct Layout {
-  size_t status_off, work_off, counters_off, part_o_off, part_lse_off, total;
+  size_t status_off, work_off, counters_off, lists_off, part_o_off, part_lse_off, total;
 };
 
 static int pick_splits(int s_q, int topk, int num_sms) {
@@ -923,13 +991,15 @@ static int pick_splits(int s_q, int topk, int num_sms) {
   return sp < 1 ? 1 : sp;
 }
 
-static Layout layout_for(int s_q, int n_splits) {
+static Layout layout_for(int s_q, int n_splits, int num_sms) {
   Layout L;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   L.status_off = 0;
   L.work_off = 4;
   L.counters_off = 256;
   size_t off = up(L.counters_off + 4 * (size_t)(s_q > 0 ? s_q : 1));
+  L.lists_off = off;
+  off = up(off + (size_t)num_sms * 2 * DSA_MAX_TOPK * 4);
   if (n_splits > 1) {
     L.part_o_off = off;
     off = up(off + (size_t)s_q * n_splits * HP * D_LAT * 4);
@@ -1001,7 +1071,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED_DEVICE;
   const int ns = pick_splits(p->s_q, p->topk, sms);
-  const Layout L = layout_for(p->s_q, ns);
+  const Layout L = layout_for(p->s_q, ns, sms);
   if (workspace_bytes < L.total) return DSA_ERR_WORKSPACE_TOO_SMALL;
 
   static int attr_done[64] = {0};
@@ -1032,6 +1102,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.counters = (uint32_t*)(ws + L.counters_off);
   K.status = (uint32_t*)(ws + L.status_off);
   K.work = (uint32_t*)(ws + L.work_off);
+  K.lists = (uint32_t*)(ws + L.lists_off);
   K.s_q = p->s_q;
   K.h_q = p->h_q;
   K.topk = p->topk;
@@ -1081,7 +1152,9 @@ int dsa_sparse_attn_num_splits(const dsa_params* p, int num_sms) {
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms) {
   const int ns = dsa_sparse_attn_num_splits(p, num_sms);
   if (ns <= 0) return 0;
-  return dsa::layout_for(p->s_q, ns).total;
+  if (num_sms <= 0) num_sms = dsa::device_sms(nullptr);
+  if (num_sms <= 0) return 0;
+  return dsa::layout_for(p->s_q, ns, num_sms).total;
 }
 
 int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp, const int32_t* indices,
