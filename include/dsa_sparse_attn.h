@@ -61,6 +61,7 @@ extern "C" {
 #define DSA_ERR_WORKSPACE_TOO_SMALL (-3)
 #define DSA_ERR_CUDA (-4)                /* CUDA runtime error (launch, attribute, memset) */
 #define DSA_ERR_UNSUPPORTED_DEVICE (-5)  /* current device is not compute capability 10.3 */
+#define DSA_ERR_SCRATCH_LIMIT (-6)       /* shape needs more than DSA_NOALLOC_SCRATCH_BYTES */
 
 #define DSA_FLAG_CHECK_INDICES 1u        /* bounds-check every index against its pool */
 
@@ -70,6 +71,7 @@ extern "C" {
 #define DSA_MAX_HEADS 64
 #define DSA_MAX_TOPK 2048
 #define DSA_ROW_BYTES 656
+#define DSA_NOALLOC_SCRATCH_BYTES (24u << 20) /* built-in scratch of the no-alloc entry */
 
 typedef struct dsa_params {
   int32_t s_q;          /* query tokens (>= 0) */
@@ -114,6 +116,34 @@ int dsa_sparse_attn_fwd_debug(const void* q, const void* kv_swa, const void* kv_
 /* Waits for `stream`, then copies the device status word (DSA_STATUS_* bits of the
  * last call that used `workspace`) into *status.  Returns DSA_OK or an error code. */
 int dsa_sparse_attn_read_status(const void* workspace, uint32_t* status, void* stream);
+
+/* Allocation-free variant of dsa_sparse_attn_fwd (the pages describe no such entry
+ * point; it exists for the library's callers).  Some callers cannot hand the kernel a
+ * workspace: serving engines that reserve almost all HBM for the KV pools at start-up
+ * and run on a fixed memory plan, plug-in hosts that pass a kernel its tensors and
+ * nothing else, and per-step code that must not call cudaMalloc or cudaFree because
+ * those synchronise the device.  This entry point uses instead a scratch array of
+ * DSA_NOALLOC_SCRATCH_BYTES (24 MiB) compiled into the library as a __device__
+ * variable: it calls no allocator of any kind.
+ *   - Same arguments and results as dsa_sparse_attn_fwd, without workspace and
+ *     workspace_bytes.  The split count and the kernel are the same.
+ *   - The first call on each device (that device current) looks up the scratch
+ *     address with cudaGetSymbolAddress; make that first call before any stream
+ *     capture.
+ *   - The scratch covers every shape whose workspace (dsa_sparse_attn_workspace_size)
+ *     is at most DSA_NOALLOC_SCRATCH_BYTES: on a 152-SM GB300 any shape with
+ *     s_q <= 5000000.  Larger shapes return DSA_ERR_SCRATCH_LIMIT with nothing
+ *     enqueued.
+ *   - The scratch header is cleared on `stream` before each launch.
+ *   - All calls on one device share the one scratch array: calls that overlap on the
+ *     GPU (different streams, not ordered by events) race and give undefined results.
+ *   - status_out (device pointer, 4-byte aligned, may be NULL) receives the call's
+ *     DSA_STATUS_* word, copied on `stream` after the kernel. */
+int dsa_sparse_attn_fwd_noalloc(const void* q, const void* kv_swa, const void* kv_cmp,
+                                const int32_t* indices, const int32_t* topk_length,
+                                const int32_t* positions, const void* norm_w,
+                                void* out_fp8, uint8_t* out_sf, const dsa_params* p,
+                                uint32_t* status_out, void* stream);
 
 /* Split count the forward call uses for a shape (exposed for tests and tooling). */
 int dsa_sparse_attn_num_splits(const dsa_params* p, int num_sms);

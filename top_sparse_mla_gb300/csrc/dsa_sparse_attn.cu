@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <mutex>
 #include <stdint.h>
 
 #include "dsa_sparse_attn.h"
@@ -1121,6 +1122,59 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   return DSA_OK;
 }
 
+// ------------------------------------------------------- allocation-free entry
+// Scratch of dsa_sparse_attn_fwd_noalloc, in place of a caller-supplied workspace.
+// It is zero-initialised device memory reserved when the module loads; its address is
+// looked up once per device and cached.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+static std::mutex g_noalloc_mutex;
+static void* g_noalloc_ptr[64];
+
+static int noalloc_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return DSA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DSA_OK;
+}
+
+static int launch_noalloc(const void* q, const void* kv_swa, const void* kv_cmp, const int32_t* indices,
+                          const int32_t* topk_length, const int32_t* positions, const void* norm_w, void* out_fp8,
+                          uint8_t* out_sf, const dsa_params* p, uint32_t* status_out, void* stream) {
+  int rc = check_params(p);
+  if (rc != DSA_OK) return rc;
+  if (status_out && !aligned(status_out, 4)) return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (p->s_q == 0) {
+    if (status_out && cudaMemsetAsync(status_out, 0, 4, st) != cudaSuccess) return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
+  int dev = 0;
+  const int sms = device_sms(&dev);
+  if (sms <= 0) return DSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DSA_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED_DEVICE;
+  const Layout L = layout_for(p->s_q, pick_splits(p->s_q, p->topk, sms), sms);
+  if (L.total > (size_t)DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(dev, &scratch);
+  if (rc != DSA_OK) return rc;
+  // launch() clears the scratch header and the combine counters on `st` first
+  rc = launch(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_w, out_fp8, out_sf, nullptr, nullptr, p,
+              scratch, DSA_NOALLOC_SCRATCH_BYTES, stream);
+  if (rc != DSA_OK) return rc;
+  if (status_out && cudaMemcpyAsync(status_out, (const uint8_t*)scratch + L.status_off, 4, cudaMemcpyDeviceToDevice,
+                                    st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
 }  // namespace dsa
 
 // ================================================================== C ABI
@@ -1172,6 +1226,14 @@ int dsa_sparse_attn_fwd_debug(const void* q, const void* kv_swa, const void* kv_
                      p, workspace, workspace_bytes, stream);
 }
 
+int dsa_sparse_attn_fwd_noalloc(const void* q, const void* kv_swa, const void* kv_cmp, const int32_t* indices,
+                                const int32_t* topk_length, const int32_t* positions, const void* norm_w,
+                                void* out_fp8, uint8_t* out_sf, const dsa_params* p, uint32_t* status_out,
+                                void* stream) {
+  return dsa::launch_noalloc(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_w, out_fp8, out_sf, p,
+                             status_out, stream);
+}
+
 int dsa_sparse_attn_read_status(const void* workspace, uint32_t* status, void* stream) {
   if (!workspace || !status) return DSA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
@@ -1188,6 +1250,8 @@ const char* dsa_error_string(int code) {
     case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (see dsa_sparse_attn_workspace_size)";
     case DSA_ERR_CUDA: return "CUDA runtime error";
     case DSA_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case DSA_ERR_SCRATCH_LIMIT:
+      return "shape needs more scratch than the no-alloc entry's built-in DSA_NOALLOC_SCRATCH_BYTES";
     default: return "unknown error";
   }
 }

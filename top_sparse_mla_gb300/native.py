@@ -19,18 +19,21 @@ DSA_ERR_UNSUPPORTED_SHAPE = -2
 DSA_ERR_WORKSPACE_TOO_SMALL = -3
 DSA_ERR_CUDA = -4
 DSA_ERR_UNSUPPORTED_DEVICE = -5
+DSA_ERR_SCRATCH_LIMIT = -6
 DSA_FLAG_CHECK_INDICES = 1
 DSA_STATUS_INDEX_OUT_OF_RANGE = 1
 DSA_STATUS_WAIT_TIMEOUT = 2
 DSA_MAX_HEADS = 64
 DSA_MAX_TOPK = 2048
 DSA_ROW_BYTES = 656
+DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 
 EXPORTED = (
     "dsa_params_init",
     "dsa_sparse_attn_workspace_size",
     "dsa_sparse_attn_fwd",
     "dsa_sparse_attn_fwd_debug",
+    "dsa_sparse_attn_fwd_noalloc",
     "dsa_sparse_attn_read_status",
     "dsa_sparse_attn_num_splits",
     "dsa_error_string",
@@ -82,6 +85,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_sparse_attn_fwd.restype = ctypes.c_int
     lib.dsa_sparse_attn_fwd_debug.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, pp, vp, sz, vp]
     lib.dsa_sparse_attn_fwd_debug.restype = ctypes.c_int
+    lib.dsa_sparse_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, pp, vp, vp]
+    lib.dsa_sparse_attn_fwd_noalloc.restype = ctypes.c_int
     lib.dsa_sparse_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.dsa_sparse_attn_read_status.restype = ctypes.c_int
     lib.dsa_error_string.argtypes = [ctypes.c_int]
@@ -148,6 +153,15 @@ def dsa_sparse_attn_fwd_debug(q, kv_swa, kv_cmp, indices, topk_length, positions
                                              int(workspace_bytes), _stream(stream))
     if rc != DSA_OK:
         raise DsaError(rc, "dsa_sparse_attn_fwd_debug")
+
+
+def dsa_sparse_attn_fwd_noalloc(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_w, out_fp8, out_sf,
+                                p: DsaParams, status_out=None, stream=None) -> None:
+    rc = library().dsa_sparse_attn_fwd_noalloc(_ptr(q), _ptr(kv_swa), _ptr(kv_cmp), _ptr(indices),
+                                               _ptr(topk_length), _ptr(positions), _ptr(norm_w), _ptr(out_fp8),
+                                               _ptr(out_sf), ctypes.byref(p), _ptr(status_out), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_sparse_attn_fwd_noalloc")
 
 
 def dsa_sparse_attn_read_status(workspace, stream=None) -> int:
