@@ -3,26 +3,25 @@
 // MXFP8 cast, in one persistent kernel (stages as named on "Deepseek V41 Attention
 // MegaKernel", vLLM PR #56344, Purpose).
 //
-// Work item = (query token, KV split), taken from a global queue.  One CTA of 16 warps
-// per SM; the warps are specialised and talk through mbarriers, so consecutive items
-// and consecutive tiles overlap:
+// Work item = (query token, KV split).  One CTA of 18 warps per SM; the warps are
+// specialised and talk through mbarriers:
 //
-//   PREP  (warps 13-14) take an item; compact its valid index columns into a row list;
-//                       rotary table; L2 prefetch of the rows; build q~ = RoPE(RMSNorm(q)
-//                       * w) in fp16 as the B operand of QK^T (K-major, 128-byte swizzle)
-//   KD    (warps 4-7)   one gathered row per thread -> fp16 K~ (fp32 scale folded) into a
-//                       TMEM ring: the A operand of QK^T, lane = row
-//   VD    (warps 0-3)   one gathered row per thread -> fp16 V~ into an SMEM ring in
-//                       MN-major layout: the A operand of PV
-//   QK    (warp 12)     S^T[128 rows x 64 heads]  = K~ . q~^T     (tcgen05, M=128 N=64)
-//   PV    (warp 15)     O^T[512 dims x 64 heads] += V~^T . P^T    (tcgen05, M=128 N=64)
-//   SM    (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P), O rescale,
-//                       then the epilogue: O / l, inverse RoPE, MXFP8 cast and stores, or
-//                       the split partials and the last split's combine
+//   DQ   (warps 0-7)   gathered rows -> fp16 latent tile [128 rows x 512 dims] in shared
+//                      memory, fp32 block scale folded in.  The one tile is the A operand
+//                      of both contractions: K-major for QK^T (M = rows), MN-major for PV
+//                      (M = dims).  The next tile's raw bytes wait in registers.
+//   SM   (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P); the rotary part
+//                      of the next tile's keys (bf16 -> fp16) into TMEM
+//   EPI  (warps 12-15) q~ = RoPE(RMSNorm(q) * w) * scale * log2(e) in fp16 as the B
+//                      operand of QK^T (fp32 statistics), built for the next item while
+//                      the current one finishes; the epilogue: O / l, inverse RoPE, MXFP8
+//                      cast and stores, or the split partials
+//   MMA  (warp 16)     S^T[128 rows x 64 heads] = K~ . q~^T; O^T[512 x 64] += V~^T . P;
+//                      l[64] += 1^T . P (row sums on the tensor core)
+//   PREP (warp 17)     take an item, compact its valid index columns into a row list, L2
+//                      prefetch of the rows and of q, rotary table
 //
-// The two MMA issuers are separate threads so that QK^T of the next tile never waits
-// behind PV of the previous one.  S^T and P are double-buffered.
-// TMEM: O^T columns 0..255, S^T double buffer 256..383, K~ ring 384..511.
+// TMEM: O^T 0..255, l 256..319, S^T 320..447 (two buffers), K~ rope part 448..511 (two).
 // Every mbarrier wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT,
 // every role leaves its loop, the tensor core is drained and TMEM freed.
 
@@ -42,55 +41,53 @@ constexpr int D_QK = 576;
 constexpr int ROW_BYTES = 656;
 constexpr int TILE = 128;           // gathered rows per tile (the M of QK^T)
 constexpr int HP = 64;              // heads as seen by the MMAs (padded)
-constexpr int NTHREADS = 512;
-constexpr int W_VD = 0, W_KD = 4, W_SM = 8, W_QK = 12, W_PREP = 13, N_PREP_WARPS = 2, W_PV = 15;
-constexpr int N_PREP = 32 * N_PREP_WARPS;
-constexpr int K_SLOTS = 4;          // TMEM ring of 32-column slots (64 dims of K~ each)
-constexpr int V_SLOTS = 3;          // SMEM ring of [128 dims x 128 rows] fp16 blocks
-constexpr int HC_PER_TILE = 9;      // 8 latent half-chunks (64 dims) + the rope chunk
+constexpr int W_SM = 8, W_EPI = 12, W_MMA = 16, W_PREP = 17;
+constexpr int NWARPS = 18;
+constexpr int NTHREADS = 32 * NWARPS;
+constexpr int N_DQ = 256, N_SM = 128, N_EPI = 128, N_PREP = 32;
 constexpr int MAX_SPLITS = 16;
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
-constexpr uint32_t TM_S = 256;      // + 64 * buffer
-constexpr uint32_t TM_K = 384;      // + 32 * slot
+constexpr uint32_t TM_L = 256;
+constexpr uint32_t TM_S = 320;      // + 64 * buffer
+constexpr uint32_t TM_KR = 448;     // + 32 * buffer
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t SM_Q = 0;                                 // q~: 9 K-atoms x 8 KB
-constexpr uint32_t SM_V = SM_Q + 9 * 8192;                   // V~ ring: 3 x 32 KB
-constexpr uint32_t SM_P = SM_V + V_SLOTS * 32768;            // P: 2 x 16 KB; epilogue slabs
-constexpr uint32_t SM_KDBUF = SM_P + 2 * 16384;              // 4 KD warps x [32 rows x 128 B]
-constexpr uint32_t SM_VDSC = SM_KDBUF + 4 * 4096;            // 4 VD warps x [32 rows x 4 scales]
-constexpr uint32_t SM_ROPE = SM_VDSC + 4 * 512;              // 2 x 32 x (cos, sin)
-constexpr uint32_t SM_ITEM = SM_ROPE + 2 * 32 * 8;           // 2 x item info (8 ints)
-constexpr uint32_t SM_NORMW = SM_ITEM + 2 * 32;              // 576 fp32
-constexpr uint32_t SM_MREF = SM_NORMW + D_QK * 4;            // 64 fp32 running max (log2 units)
-constexpr uint32_t SM_LACC = SM_MREF + 256;                  // 64 fp32 running sum
-constexpr uint32_t SM_ALPHA = SM_LACC + 256;                 // 64 fp32 rescale / 1/l
-constexpr uint32_t SM_RED = SM_ALPHA + 256;                  // 4 warps x 64 fp32
-constexpr uint32_t SM_LPART = SM_RED + 1024;                 // 2 x 4 warps x 64 fp32 row sums
-constexpr uint32_t SM_FLAG = SM_LPART + 2048;                // 2 x 4 fp32
-constexpr uint32_t SM_MISC = SM_FLAG + 32;                   // misc ints
-constexpr uint32_t SM_BAR = SM_MISC + 64;                    // mbarriers
+constexpr uint32_t SM_Q = 0;                       // q~: 9 K-atoms x [64 heads x 128 B]
+constexpr uint32_t SM_V = SM_Q + 9 * 8192;         // latent tile: 4 chunks x 2 halves x 16 KB
+constexpr uint32_t SM_P = SM_V + 4 * 32768;        // P: [128 rows x 64 heads] fp16
+constexpr uint32_t SM_ONES = SM_P + 16384;         // [128 x 16] fp16 ones (A of the row sums)
+constexpr uint32_t SM_NORMW = SM_ONES + 4096;      // 576 bf16
+constexpr uint32_t SM_ROPE = SM_NORMW + 1152;      // 2 x 32 x (cos, sin)
+constexpr uint32_t SM_INV = SM_ROPE + 512;         // 2 x 64 fp32: scale * log2(e) / rms(q)
+constexpr uint32_t SM_ITEM = SM_INV + 512;         // 2 x 8 ints
+constexpr uint32_t SM_M = SM_ITEM + 64;            // 64 fp32 running max (log2 units)
+constexpr uint32_t SM_ALPHA = SM_M + 256;          // 64 fp32 rescale factors
+constexpr uint32_t SM_MFIN = SM_ALPHA + 256;       // 2 x 64 fp32 final max per item
+constexpr uint32_t SM_RED = SM_MFIN + 512;         // 4 warps x 64 fp32
+constexpr uint32_t SM_ESCL = SM_RED + 1024;        // 4 EPI warps x 32 fp32 block scales
+constexpr uint32_t SM_EL = SM_ESCL + 512;          // 64 fp32 row sums, then 1/l
+constexpr uint32_t SM_ELSE = SM_EL + 256;          // 64 fp32 LSE (log2 units)
+constexpr uint32_t SM_FLAG = SM_ELSE + 256;        // 2 x 4 fp32
+constexpr uint32_t SM_MISC = SM_FLAG + 32;         // misc ints
+constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
 constexpr uint32_t SM_END = SM_BAR + 48 * 8;
-constexpr uint32_t SMEM_BYTES = SM_END + 1024;               // + alignment slack
-// the epilogue reuses the two P buffers: one [64 heads x 32 dims] fp32 slab per SM warp
-// (rows of 128 bytes, 16-byte chunks XOR-swizzled by row), the combine weights after it
-constexpr uint32_t EPI_SLAB_BYTES = HP * 32 * 4;
-constexpr uint32_t SM_CW = SM_P;                             // MAX_SPLITS x 64 fp32 (combine)
-static_assert(4 * EPI_SLAB_BYTES <= 2 * 16384, "epilogue slabs fit in the P buffers");
+constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// after the last item the latent tile area holds the split-combine weights
+constexpr uint32_t SM_CW = SM_V;
 
 enum {
-  B_KFULL = 0, B_KEMPTY = B_KFULL + K_SLOTS, B_VFULL = B_KEMPTY + K_SLOTS, B_VEMPTY = B_VFULL + V_SLOTS,
-  B_SFULL = B_VEMPTY + V_SLOTS, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2,
-  B_ITFULL = B_PEMPTY + 2, B_ITEMPTY = B_ITFULL + 2,
-  B_ODONE = B_ITEMPTY + 2, B_OFREE, B_QREADY, B_QFREE, B_GRP, B_PREP, B_DRAIN, B_COUNT
+  B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
+  B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
+  B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_ODONE = B_ITEMPTY + 2, B_OFREE,
+  B_QREADY = B_OFREE + 4, B_QFREE, B_MFIN, B_SMG, B_EPG, B_DRAIN, B_COUNT
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
-enum { M_TMEM = 0, M_ABORT, M_LAST };                           // misc ints
+enum { M_TMEM = 0, M_ABORT, M_LAST, M_TOKEN };                   // misc ints
 enum { IT_ITEM = 0, IT_TOKEN, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS }; // item info ints
 
 struct KParams {
@@ -105,7 +102,7 @@ struct KParams {
   uint8_t* out_sf;
   float* out_precast;
   float* out_lse;
-  float* part_o;        // [s_q][n_splits][64][512]
+  float* part_o;        // [s_q][n_splits][64 heads][512 dims]
   float* part_lse;      // [s_q][n_splits][64] (log2 units)
   uint32_t* counters;   // [s_q] split arrivals
   uint32_t* status;
@@ -157,432 +154,595 @@ DSA_DEV bool wait_bar_w(const Ctx& c, int b, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// Group barrier of one role on an mbarrier (bounded, unlike bar.sync).
+struct Group {
+  int b;
+  uint32_t n;
+  DSA_DEV bool sync(const Ctx& c) {
+    mbar_arrive(bar(c, b));
+    const bool ok = wait_bar_w(c, b, n & 1);
+    ++n;
+    return ok;
+  }
+};
+
 DSA_DEV const uint8_t* row_ptr(const KParams& P, uint32_t e) {
   const uint8_t* base = (e & 0x80000000u) ? P.kv_cmp : P.kv_swa;
   return base + (size_t)(e & 0x7FFFFFFFu) * ROW_BYTES;
 }
+DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
+  return P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
+}
+DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 8 * b; }
+
+// Reduce 32 per-lane values across the warp, one result per value: afterwards lane L
+// holds the reduction of value L in v[0].
+template <bool IS_MAX>
+DSA_DEV void reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int k = 16, n = 32; k >= 1; k >>= 1, n >>= 1) {
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, k);
+      v[i] = IS_MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
 
 // ================================================================== PREP
-// Scan, rotary table, prefetch and q~ for every item, one item ahead of the others.
-DSA_DEV void prep_role(const KParams& P, const Ctx& c, int pw, int lane) {
-  const int pt = pw * 32 + lane;
+// Items, row lists and rotary tables, one item ahead of the other roles.
+DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
-  // volatile: re-read per head group instead of 72 weights held in registers
-  const volatile float* s_normw = reinterpret_cast<const volatile float*>(c.sm + SM_NORMW);
-  uint32_t n_prep_sync = 0;
-  auto prep_sync = [&]() -> bool {
-    mbar_arrive(bar(c, B_PREP));
-    const bool r = wait_bar_w(c, B_PREP, n_prep_sync & 1);
-    ++n_prep_sync;
-    return r;
-  };
+  const bool split_path = P.n_splits > 1;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
     int* info = s_items + 8 * b;
     if (!wait_bar_w(c, B_ITEMPTY + b, ((seq >> 1) & 1) ^ 1)) return;
-    if (pt == 0) {
-      const int item = (int)atomicAdd(P.work, 1u);
-      info[IT_ITEM] = item < P.n_items ? item : -1;
+    int item = 0;
+    if (lane == 0) {
+      // split path: exactly one item per CTA (the grid has one CTA per item), so the
+      // last split of a token can run its combine with the whole CTA afterwards
+      if (split_path) item = seq == 0 ? (int)blockIdx.x : P.n_items;
+      else item = (int)atomicAdd(P.work, 1u);
+      item = item < P.n_items ? item : -1;
     }
-    if (!prep_sync()) return;
-    const int item = info[IT_ITEM];
+    item = __shfl_sync(0xFFFFFFFFu, item, 0);
     if (item < 0) {
+      if (lane == 0) info[IT_ITEM] = -1;
       mbar_arrive(bar(c, B_ITFULL + b));   // tells every role to stop
       return;
     }
     const int t = item / P.n_splits;
     const int split = item % P.n_splits;
-    if (pw == 0) {
-      // compact the valid columns (j < topk_length, index >= 0), 256 indices per load batch
-      uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
-      int L = P.topk_length[t];
-      L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
-      const int32_t* irow = P.indices + (size_t)t * P.topk;
-      int count = 0;
-      for (int base = 0; base < L; base += 256) {
-        int v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int j = base + 32 * k + lane;
-          v[k] = (j < L) ? __ldg(irow + j) : -1;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int j = base + 32 * k + lane;
-          const bool cmp = j >= P.n_swa_cols;
-          bool valid = v[k] >= 0;
-          if (valid && (P.flags & DSA_FLAG_CHECK_INDICES)) {
-            const long long nr = cmp ? P.n_cmp_rows : P.n_swa_rows;
-            if ((long long)v[k] >= nr) {
-              valid = false;
-              atomicOr(P.status, DSA_STATUS_INDEX_OUT_OF_RANGE);
-            }
-          }
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid);
-          if (valid) list[count + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
-          count += __popc(bal);
-        }
-      }
-      const int n_tiles_tok = (count + TILE - 1) / TILE;
-      const int tps = (n_tiles_tok + P.n_splits - 1) / P.n_splits;
-      const int tile0 = split * tps;
-      int tile1 = tile0 + tps;
-      if (tile1 > n_tiles_tok) tile1 = n_tiles_tok;
-      const int T = tile1 > tile0 ? tile1 - tile0 : 0;
-      const int row0 = tile0 * TILE;
-      const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
-      __syncwarp();
-      for (int r = lane; r < nrows; r += 32) prefetch_l2(row_ptr(P, list[row0 + r]), ROW_BYTES);
-      if (lane == 0) {
-        info[IT_TOKEN] = t;
-        info[IT_SPLIT] = split;
-        info[IT_T] = T;
-        info[IT_ROW0] = row0;
-        info[IT_NROWS] = nrows;
-      }
-    } else {
-      // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
+    // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
+    {
       float2* rope = reinterpret_cast<float2*>(c.sm + SM_ROPE) + 32 * b;
       const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[lane];
       const float frac = (float)(turns >> 40) * 5.9604644775390625e-08f;   // top 24 bits / 2^24
       float sn, cs;
       sincospif(2.0f * frac, &sn, &cs);
       rope[lane] = make_float2(cs, sn);
-      if (lane == 0) prefetch_l2(P.q + (size_t)t * P.h_q * D_QK, (uint32_t)(P.h_q * D_QK * 2));
     }
-    if (!prep_sync()) return;
-    mbar_arrive(bar(c, B_ITFULL + b));   // rows, table and tile range published
-
-    // q~ for this item, once the previous item's QK^T no longer reads the buffer.
-    // Eight lanes per head, four heads per warp at a time, the next four heads' loads
-    // in flight while the current ones are normalised and stored.
-    if (!wait_bar_w(c, B_QFREE, (seq & 1) ^ 1)) return;
-    if (info[IT_T] > 0) {
-      const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-      const float eps = P.rms_eps;
-      const int sub = lane >> 3, sl = lane & 7;     // head slot within the group, lane within the head
-      uint4 raw[2][9];
-      auto load_group = [&](int h0, uint4 (&dst)[9]) {
-        const int h = h0 + sub;
+    // q[t] is read twice soon after (statistics, then q~)
+    if (lane < 8) {
+      const uint32_t bytes = (uint32_t)(P.h_q * D_QK * 2);
+      const uint32_t part = ((bytes / 8) + 15) & ~15u;
+      const uint32_t off = part * (uint32_t)lane;
+      if (off < bytes) prefetch_l2(reinterpret_cast<const uint8_t*>(P.q + (size_t)t * P.h_q * D_QK) + off,
+                                   off + part <= bytes ? part : bytes - off);
+    }
+    // compact the valid columns (j < topk_length, index >= 0), 256 indices per load batch
+    uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
+    int L = P.topk_length[t];
+    L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
+    const int32_t* irow = P.indices + (size_t)t * P.topk;
+    int count = 0;
+    for (int base = 0; base < L; base += 256) {
+      int v[8];
 #pragma unroll
-        for (int k = 0; k < 9; ++k)
-          dst[k] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + (sl + 8 * k) * 8)
-                               : make_uint4(0, 0, 0, 0);
-      };
-      // warp pw builds heads [32 pw, 32 pw + 32), four at a time
-      auto process = [&](const uint4 (&cur)[9], int it) {
-        const int h = 32 * pw + 4 * it + sub;
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-          const uint32_t w4[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = __uint_as_float(w4[e] << 16), bb = __uint_as_float(w4[e] & 0xFFFF0000u);
-            ss = fmaf(a, a, fmaf(bb, bb, ss));
-          }
-        }
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
-        const float inv = rsqrtf(ss * (1.0f / D_QK) + eps);
-        const bool live = h < P.h_q;
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-          const int ch = sl + 8 * k;           // 16-byte chunk of the head row (8 dims)
-          const uint32_t w4[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[2 * e] = __uint_as_float(w4[e] << 16) * inv * s_normw[ch * 8 + 2 * e];
-            x[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u) * inv * s_normw[ch * 8 + 2 * e + 1];
-          }
-          if (k == 8) {                         // chunks 64..71: the rotary dims 512..575
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 r = rope[(ch - 64) * 4 + e];
-              const float x0 = x[2 * e], x1 = x[2 * e + 1];
-              x[2 * e] = x0 * r.x - x1 * r.y;
-              x[2 * e + 1] = x0 * r.y + x1 * r.x;
-            }
-          }
-          uint4 o;
-          o.x = pack_f16x2(x[0], x[1]);
-          o.y = pack_f16x2(x[2], x[3]);
-          o.z = pack_f16x2(x[4], x[5]);
-          o.w = pack_f16x2(x[6], x[7]);
-          if (!live) o = make_uint4(0, 0, 0, 0);
-          const uint32_t atom = ch >> 3, cc = ch & 7;
-          sts128(c.sb + SM_Q + atom * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((cc ^ (h & 7)) << 4), o);
-        }
-      };
-      load_group(32 * pw, raw[0]);
-#pragma unroll 1
-      for (int it = 0; it < 8; it += 2) {
-        load_group(32 * pw + 4 * (it + 1), raw[1]);
-        process(raw[0], it);
-        if (it + 2 < 8) load_group(32 * pw + 4 * (it + 2), raw[0]);
-        process(raw[1], it + 1);
+      for (int k = 0; k < 8; ++k) {
+        const int j = base + 32 * k + lane;
+        v[k] = (j < L) ? __ldg(irow + j) : -1;
       }
-      fence_async_smem();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int j = base + 32 * k + lane;
+        const bool cmp = j >= P.n_swa_cols;
+        bool valid = v[k] >= 0;
+        if (valid && (P.flags & DSA_FLAG_CHECK_INDICES)) {
+          const long long nr = cmp ? P.n_cmp_rows : P.n_swa_rows;
+          if ((long long)v[k] >= nr) {
+            valid = false;
+            atomicOr(P.status, DSA_STATUS_INDEX_OUT_OF_RANGE);
+          }
+        }
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid);
+        if (valid) list[count + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
+        count += __popc(bal);
+      }
     }
-    mbar_arrive(bar(c, B_QREADY));
+    const int n_tiles_tok = (count + TILE - 1) / TILE;
+    const int tps = (n_tiles_tok + P.n_splits - 1) / P.n_splits;
+    const int tile0 = split * tps;
+    int tile1 = tile0 + tps;
+    if (tile1 > n_tiles_tok) tile1 = n_tiles_tok;
+    const int T = tile1 > tile0 ? tile1 - tile0 : 0;
+    const int row0 = tile0 * TILE;
+    const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
+    __syncwarp();
+    for (int r = lane; r < nrows; r += 32) prefetch_l2(row_ptr(P, list[row0 + r]), ROW_BYTES);
+    if (lane == 0) {
+      info[IT_ITEM] = item;
+      info[IT_TOKEN] = t;
+      info[IT_SPLIT] = split;
+      info[IT_T] = T;
+      info[IT_ROW0] = row0;
+      info[IT_NROWS] = nrows;
+    }
+    mbar_arrive(bar(c, B_ITFULL + b));   // rows, tile range, rotary table
   }
 }
 
-// ================================================================== QK issuer
-DSA_DEV void qk_role(const KParams& P, const Ctx& c, uint32_t tmem) {
-  constexpr uint32_t IDESC_QK = idesc_f16(128, HP, 0, 0);
-  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  uint32_t kq = 0, g = 0;
-  for (uint32_t seq = 0;; ++seq) {
-    const int b = seq & 1;
-    const int* info = s_items + 8 * b;
-    if (!wait_bar(c, B_ITFULL + b, (seq >> 1) & 1)) return;
-    const int item = info[IT_ITEM];
-    const int T = info[IT_T];
-    mbar_arrive(bar(c, B_ITEMPTY + b));
-    if (item < 0) return;
-    if (!wait_bar(c, B_QREADY, seq & 1)) return;
-    tc_fence_after();
-    for (int tt = 0; tt < T; ++tt) {
-      const uint32_t sb = g & 1;
-      if (!wait_bar(c, B_SEMPTY + sb, ((g >> 1) & 1) ^ 1)) return;
-      tc_fence_after();
-      for (int hc = 0; hc < HC_PER_TILE; ++hc) {
-        const uint32_t slot = kq % K_SLOTS;
-        if (!wait_bar(c, B_KFULL + slot, (kq / K_SLOTS) & 1)) return;
-        tc_fence_after();
+// ================================================================== DQ
+// Lane (sub, ch) of warp w converts 16 bytes (16 dims) of rows 16 w + 4 k + sub,
+// k = 0..3, per 128-dim chunk: eight lanes read 128 contiguous bytes of a row.  The
+// fp16 values go straight into the 128-byte-swizzled tile (rows of 128 bytes holding 64
+// dims); the four rows of one store instruction alternate in row parity, which keeps the
+// stores free of bank conflicts.  Raw bytes are loaded two chunks ahead of their
+// conversion (chunk c of a tile lives in register slot c % 2).
+struct DqRows {
+  uint32_t e[4];   // list entries of rows 16 w + 4 k + sub
+  bool v[4];
+  uint32_t es;     // lanes ch < 4: entry of row 16 w + 4 ch + sub (its scales)
+  bool vs;
+};
+
+DSA_DEV void dq_load_rows(const uint32_t* list, int tt, int nrows, int w, int sub, int ch, DqRows& R) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = sdesc(c.sb + SM_Q + hc * 8192 + kk * 32, 16, 1024);
-          mma_ts(tmem + TM_S + 64 * sb, tmem + TM_K + 32 * slot + 8 * kk, bd, IDESC_QK, (hc | kk) ? 1u : 0u);
-        }
-        tc_commit(bar(c, B_KEMPTY + slot));
-        ++kq;
+  for (int k = 0; k < 4; ++k) {
+    const int r = tt * TILE + 16 * w + 4 * k + sub;
+    R.v[k] = r < nrows;
+    R.e[k] = R.v[k] ? __ldcg(list + r) : 0u;
+  }
+  const int rs = tt * TILE + 16 * w + 4 * (ch & 3) + sub;
+  R.vs = ch < 4 && rs < nrows;
+  R.es = R.vs ? __ldcg(list + rs) : 0u;
+}
+
+DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const DqRows& R, int ch) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    dst[k] = R.v[k] ? ldg_nc(row_ptr(P, R.e[k]) + 128 * cidx + 16 * ch) : make_uint4(0, 0, 0, 0);
+}
+
+DSA_DEV uint4 dq_load_scales(const KParams& P, const DqRows& R) {
+  return R.vs ? ldg_nc(row_ptr(P, R.es) + D_LAT) : make_uint4(0, 0, 0, 0);
+}
+
+DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
+  const int sub = lane >> 3, ch = lane & 7;
+  const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
+  const uint32_t c0 = (uint32_t)(2 * (ch & 3));
+  uint4 raw[2][4];
+  uint4 scl;
+  DqRows cur, nxt;
+  uint32_t g = 0, seq = 0;
+  // next item with tiles: its info waited for, rows of tile 0 and its first two chunks
+  // in flight
+  auto open_item = [&]() -> int {   // 1 = opened, 0 = no more items, -1 = aborted
+    while (true) {
+      const int b = seq & 1;
+      if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return -1;
+      const int* info = item_info(c, b);
+      if (info[IT_ITEM] < 0) return 0;
+      if (info[IT_T] > 0) {
+        dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, ch, cur);
+        scl = dq_load_scales(P, cur);
+        dq_load_chunk(P, raw[0], 0, cur, ch);
+        dq_load_chunk(P, raw[1], 1, cur, ch);
+        return 1;
       }
-      tc_commit(bar(c, B_SFULL + sb));
+      mbar_arrive(bar(c, B_ITEMPTY + b));
+      ++seq;
+    }
+  };
+  if (open_item() <= 0) return;
+  while (true) {
+    const int b = seq & 1;
+    const int* info = item_info(c, b);
+    const int T = info[IT_T], nrows = info[IT_NROWS];
+    const uint32_t* list = item_list(P, b) + info[IT_ROW0];
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      const bool more = tt + 1 < T;
+      if (more) dq_load_rows(list, tt + 1, nrows, w, sub, ch, nxt);
+#pragma unroll
+      for (int cidx = 0; cidx < 4; ++cidx) {
+        if (!wait_bar_w(c, B_VFREE + cidx, (g & 1) ^ 1)) return;
+        const uint32_t cbase = c.sb + SM_V + (uint32_t)cidx * 32768 + half_off;
+        const uint32_t sc = cidx == 0 ? scl.x : cidx == 1 ? scl.y : cidx == 2 ? scl.z : scl.w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float sv = __uint_as_float(__shfl_sync(0xFFFFFFFFu, sc, sub * 8 + k));
+          uint32_t o[8];
+          dequant16(raw[cidx & 1][k], __float2half2_rn(sv), o);
+          const uint32_t row = (uint32_t)(16 * w + 4 * k + sub);
+          const uint32_t rsw = row & 7;
+          const uint32_t rb = cbase + (row >> 3) * 1024 + rsw * 128;
+          sts128(rb + ((c0 ^ rsw) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+          sts128(rb + (((c0 + 1) ^ rsw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+        }
+        fence_async_smem();
+        mbar_arrive(bar(c, B_VFULL + cidx));
+        // the chunk two ahead
+        if (cidx < 2) dq_load_chunk(P, raw[cidx & 1], cidx + 2, cur, ch);
+        else if (more) dq_load_chunk(P, raw[cidx & 1], cidx - 2, nxt, ch);
+      }
+      if (more) {
+        scl = dq_load_scales(P, nxt);
+        cur = nxt;
+      }
       ++g;
     }
-    tc_commit(bar(c, B_QFREE));   // once per item: q~ may be rebuilt after these MMAs
+    mbar_arrive(bar(c, B_ITEMPTY + b));
+    ++seq;
+    if (open_item() <= 0) return;
   }
 }
 
-// ================================================================== PV issuer
-DSA_DEV void pv_role(const KParams& P, const Ctx& c, uint32_t tmem) {
+// ================================================================== MMA issuer
+DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
+  constexpr uint32_t IDESC_QK = idesc_f16(128, HP, 0, 0);
   constexpr uint32_t IDESC_PV = idesc_f16(128, HP, 1, 1);
-  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  uint32_t vq = 0, g = 0, n_ot = 0;
+  constexpr uint32_t IDESC_L = idesc_f16(128, HP, 0, 1);
+  const uint64_t ones_desc = sdesc_noswz(c.sb + SM_ONES, 128, 256);
+  uint32_t g = 0, nq = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
-    const int* info = s_items + 8 * b;
     if (!wait_bar(c, B_ITFULL + b, (seq >> 1) & 1)) return;
+    const int* info = item_info(c, b);
     const int item = info[IT_ITEM];
     const int T = info[IT_T];
     mbar_arrive(bar(c, B_ITEMPTY + b));
     if (item < 0) return;
+    if (T == 0) continue;
+    if (!wait_bar(c, B_QREADY, nq & 1)) return;
+    tc_fence_after();
     for (int tt = 0; tt < T; ++tt) {
-      if (tt == 0) {
-        // the previous item's epilogue must have read O^T before it is overwritten
-        if (n_ot > 0 && !wait_bar(c, B_OFREE, (n_ot - 1) & 1)) return;
-        ++n_ot;
-      }
-      const uint32_t pb = g & 1;
-      if (!wait_bar(c, B_PFULL + pb, (g >> 1) & 1)) return;
-      tc_fence_after();
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t slot = vq % V_SLOTS;
-        if (!wait_bar(c, B_VFULL + slot, (vq / V_SLOTS) & 1)) return;
+      // ---- S^T = K~ . q~^T
+      const uint32_t sb = g & 1;
+      const uint32_t d_s = tmem + TM_S + 64 * sb;
+      if (!wait_bar(c, B_SFREE + sb, ((g >> 1) & 1) ^ 1)) return;
+      for (int cidx = 0; cidx < 4; ++cidx) {
+        if (!wait_bar(c, B_VFULL + cidx, g & 1)) return;
         tc_fence_after();
-        const uint32_t vbase = c.sb + SM_V + slot * 32768;
-        const uint32_t pbase = c.sb + SM_P + pb * 16384;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc(vbase + kk * 2048, 16384, 1024);
-          const uint64_t bd = sdesc(pbase + kk * 2048, 16384, 1024);
-          mma_ss(tmem + TM_O + 64 * j, ad, bd, IDESC_PV, (tt == 0 && kk == 0) ? 0u : 1u);
+          const uint32_t aoff = SM_V + cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint32_t boff = SM_Q + (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
+          mma_ss(d_s, sdesc(c.sb + aoff, 16, 1024), sdesc(c.sb + boff, 16, 1024), IDESC_QK, (cidx | kk) ? 1u : 0u);
         }
-        tc_commit(bar(c, B_VEMPTY + slot));
-        ++vq;
       }
-      tc_commit(bar(c, B_PEMPTY + pb));
+      if (!wait_bar(c, B_KRFULL + sb, (g >> 1) & 1)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts(d_s, tmem + TM_KR + 32 * sb + 8 * kk, sdesc(c.sb + SM_Q + 8 * 8192 + kk * 32, 16, 1024), IDESC_QK, 1u);
+      tc_commit(bar(c, B_SFULL + sb));
+      tc_commit(bar(c, B_KRFREE + sb));
+      if (tt == T - 1) tc_commit(bar(c, B_QFREE));   // q~ may be rebuilt after these MMAs
+      // ---- O^T += V~^T . P, l += 1^T . P
+      if (!wait_bar(c, B_PFULL, g & 1)) return;
+      tc_fence_after();
+      for (int cidx = 0; cidx < 4; ++cidx) {
+        if (tt == 0 && nq > 0) {
+          // the previous item's epilogue has read this part of O^T (and l)
+          if (!wait_bar(c, B_OFREE + cidx, (nq - 1) & 1)) return;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc(c.sb + SM_V + cidx * 32768 + kk * 2048, 16384, 1024);
+          const uint64_t bd = sdesc(c.sb + SM_P + kk * 2048, 16384, 1024);
+          mma_ss(tmem + TM_O + 64 * cidx, ad, bd, IDESC_PV, (tt == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(bar(c, B_VFREE + cidx));
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t bd = sdesc(c.sb + SM_P + kk * 2048, 16384, 1024);
+        mma_ss(tmem + TM_L, ones_desc, bd, IDESC_L, (tt == 0 && kk == 0) ? 0u : 1u);
+      }
+      tc_commit(bar(c, B_PFREE));
       if (tt == T - 1) tc_commit(bar(c, B_ODONE));
       ++g;
     }
+    ++nq;
   }
 }
 
-// ================================================================== KD
-// Rows reach the SM with coalesced loads (eight lanes read 128 contiguous bytes of a
-// row), pass through a per-warp shared-memory transpose (16-byte chunks XOR-swizzled by
-// row) and leave one row per thread, which is what a 32x32b TMEM store needs.
-DSA_DEV void kd_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
+// ================================================================== SM
+// One row of the tile per thread (TMEM lane = row).  Softmax of tile g, then the
+// rotary part of the keys of the next tile, which QK^T needs after PV of tile g.
+DSA_DEV void sm_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
+                     int nrows, int r, uint32_t gk) {
+  const bool valid = tt * TILE + r < nrows;
+  uint4 raw[8];
+  const uint8_t* src = valid ? row_ptr(P, __ldcg(list + tt * TILE + r)) + D_LAT + 16 : nullptr;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) raw[k] = valid ? ldg_nc(src + 16 * k) : make_uint4(0, 0, 0, 0);
+  uint32_t v[32];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[4 * k + 0] = bf16x2_to_f16x2(raw[k].x);
+    v[4 * k + 1] = bf16x2_to_f16x2(raw[k].y);
+    v[4 * k + 2] = bf16x2_to_f16x2(raw[k].z);
+    v[4 * k + 3] = bf16x2_to_f16x2(raw[k].w);
+  }
+  const uint32_t kb = gk & 1;
+  if (!wait_bar_w(c, B_KRFREE + kb, ((gk >> 1) & 1) ^ 1)) return;
+  tc_fence_after();
+  tmem_st32(tmem + tlane + TM_KR + 32 * kb, v);
+  tc_wait_st();
+  tc_fence_before();
+  mbar_arrive(bar(c, B_KRFULL + kb));
+}
+
+DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
+  const int r = q4 * 32 + lane;
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
-  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  const uint32_t xb = c.sb + SM_KDBUF + q4 * 4096;       // this warp's transpose buffer
-  const int sub = lane >> 3, ch = lane & 7;             // loader view: row 4k + sub, chunk ch
-  uint32_t kq = 0;
-  for (uint32_t seq = 0;; ++seq) {
+  float* s_m = reinterpret_cast<float*>(c.sm + SM_M);
+  float* s_alpha = reinterpret_cast<float*>(c.sm + SM_ALPHA);
+  float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
+  float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
+  Group grp{B_SMG, 0};
+  uint32_t g = 0, seq = 0;
+  // next item with tiles: its info waited for and the rope of its tile 0 converted
+  auto open_item = [&]() -> int {
+    while (true) {
+      const int b = seq & 1;
+      if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return -1;
+      const int* info = item_info(c, b);
+      if (info[IT_ITEM] < 0) return 0;
+      if (info[IT_T] > 0) {
+        sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g);
+        return c.misc[M_ABORT] ? -1 : 1;
+      }
+      mbar_arrive(bar(c, B_ITEMPTY + b));
+      ++seq;
+    }
+  };
+  if (open_item() <= 0) return;
+  while (true) {
     const int b = seq & 1;
-    const int* info = s_items + 8 * b;
-    if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
-    if (info[IT_ITEM] < 0) return;
-    const int T = info[IT_T], row0 = info[IT_ROW0], nrows = info[IT_NROWS];
-    const uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
+    const int* info = item_info(c, b);
+    const int T = info[IT_T], nrows = info[IT_NROWS];
+    const uint32_t* list = item_list(P, b) + info[IT_ROW0];
+    if (r < 64) s_m[r] = -INFINITY;
+    if (!grp.sync(c)) return;
+#pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
-      const int r = q4 * 32 + lane;                     // this thread's row (TMEM lane)
-      const bool valid = tt * TILE + r < nrows;
-      const uint32_t entry = valid ? __ldg(list + row0 + tt * TILE + r) : 0u;
-      const uint8_t* my = row_ptr(P, entry);
-      __half2 s2[4];
-      {
-        const uint4 sc = valid ? ldg_nc(my + D_LAT) : make_uint4(0, 0, 0, 0);
-        s2[0] = __float2half2_rn(__uint_as_float(sc.x));
-        s2[1] = __float2half2_rn(__uint_as_float(sc.y));
-        s2[2] = __float2half2_rn(__uint_as_float(sc.z));
-        s2[3] = __float2half2_rn(__uint_as_float(sc.w));
-      }
-      // the eight rows this lane loads from
-      const uint8_t* src[8];
-      bool sv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t e = __shfl_sync(0xFFFFFFFFu, entry, 4 * k + sub);
-        sv[k] = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, 4 * k + sub) != 0;
-        src[k] = row_ptr(P, e) + 16 * ch;
-      }
-      // five 128-byte batches per row: latent 0..3, then the rope bytes 528..655
-      auto load_batch = [&](int bt, uint4 (&L)[8]) {
-        const int off = bt < 4 ? 128 * bt : 528;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) L[k] = sv[k] ? ldg_nc(src[k] + off) : make_uint4(0, 0, 0, 0);
-      };
-      uint4 L[8];
-      load_batch(0, L);
-#pragma unroll
-      for (int bt = 0; bt < 5; ++bt) {
-        // stage the batch: row (4k + sub) chunk ch -> swizzled slot
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t row = 4 * k + sub;
-          sts128(xb + row * 128 + (((uint32_t)ch ^ (row & 7)) << 4), L[k]);
-        }
-        __syncwarp();
-        if (bt < 4) load_batch(bt + 1, L);                // next batch in flight
-        const int nhalf = bt < 4 ? 2 : 1;
-#pragma unroll
+      const uint32_t sb = g & 1;
+      const uint32_t ts = tmem + tlane + TM_S + 64 * sb;
+      const bool valid = r < nrows - tt * TILE;
+      if (!wait_bar_w(c, B_SFULL + sb, (g >> 1) & 1)) return;
+      tc_fence_after();
+      bool need = tt == 0;
+      if (!need) {
+        // pass 1: how far does this tile exceed the reference max of each head?
+        float dmax = -INFINITY;
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
-          if (hf >= nhalf) break;
-          uint32_t v[32];
-          if (bt < 4) {
+          uint32_t a[32];
+          tmem_ld32(ts + 32 * hf, a);
+          const float4* m4 = reinterpret_cast<const float4*>(s_m + 32 * hf);
+          float m[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              const uint32_t chunk = (uint32_t)(4 * hf + i);
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                           : "r"(xb + (uint32_t)lane * 128 + ((chunk ^ ((uint32_t)lane & 7)) << 4)));
-              dequant16(w, s2[bt], v + 8 * i);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              uint4 w;
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                           : "r"(xb + (uint32_t)lane * 128 + (((uint32_t)i ^ ((uint32_t)lane & 7)) << 4)));
-              v[4 * i + 0] = bf16x2_to_f16x2(w.x);
-              v[4 * i + 1] = bf16x2_to_f16x2(w.y);
-              v[4 * i + 2] = bf16x2_to_f16x2(w.z);
-              v[4 * i + 3] = bf16x2_to_f16x2(w.w);
-            }
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = m4[q];
+            m[4 * q] = f.x; m[4 * q + 1] = f.y; m[4 * q + 2] = f.z; m[4 * q + 3] = f.w;
           }
-          const uint32_t slot = kq % K_SLOTS;
-          if (!wait_bar_w(c, B_KEMPTY + slot, ((kq / K_SLOTS) & 1) ^ 1)) return;
-          tc_fence_after();
-          tmem_st32(tmem + tlane + TM_K + 32 * slot, v);
-          tc_wait_st();
-          tc_fence_before();
-          mbar_arrive(bar(c, B_KFULL + slot));
-          ++kq;
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dmax = fmaxf(dmax, (valid ? __uint_as_float(a[i]) : -INFINITY) - m[i]);
         }
-        __syncwarp();                                   // buffer free for the next batch
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xFFFFFFFFu, dmax, o));
+        if (lane == 0) s_flag[4 * (g & 1) + q4] = dmax;
+        if (!grp.sync(c)) return;
+        const float* fl = s_flag + 4 * (g & 1);
+        need = !(fmaxf(fmaxf(fl[0], fl[1]), fmaxf(fl[2], fl[3])) <= 8.0f);
+      }
+      if (need) {
+        // exact tile max per head, new reference max, rescale factors
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t a[32];
+          tmem_ld32(ts + 32 * hf, a);
+          tc_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(a[i]) : -INFINITY;
+          reduce32<true>(v, lane);
+          s_red[q4 * 64 + 32 * hf + lane] = v[0];
+        }
+        if (!grp.sync(c)) return;
+        if (r < 64) {
+          const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
+          const float mo = s_m[r];
+          const float mn = fmaxf(mo, tm);
+          s_m[r] = mn;
+          s_alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+        }
+        if (!grp.sync(c)) return;
+      }
+      // the P buffer is free once PV of the previous tile has completed
+      if (!wait_bar_w(c, B_PFREE, (g & 1) ^ 1)) return;
+      // pass 2: P = exp2(S - m) in fp16, row r of the MN-major B operand
+      const uint32_t prow = c.sb + SM_P + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t a[32];
+        tmem_ld32(ts + 32 * hf, a);
+        const float4* m4 = reinterpret_cast<const float4*>(s_m + 32 * hf);
+        float m[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 f = m4[q];
+          m[4 * q] = f.x; m[4 * q + 1] = f.y; m[4 * q + 2] = f.z; m[4 * q + 3] = f.w;
+        }
+        tc_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = valid ? __uint_as_float(a[2 * i]) : -INFINITY;
+          const float x1 = valid ? __uint_as_float(a[2 * i + 1]) : -INFINITY;
+          pk[i] = pack_f16x2(exp2f(x0 - m[2 * i]), exp2f(x1 - m[2 * i + 1]));
+        }
+        const uint32_t rsw = (uint32_t)(r & 7);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t chunk = (uint32_t)(4 * hf + cc);
+          sts128(prow + ((chunk ^ rsw) << 4), make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(c, B_SFREE + sb));     // S^T fully read
+      if (need && tt > 0) {
+        // O^T and l rescaled (PV of the previous tile has completed: PFREE above)
+        tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < 10; ++j) {
+          uint32_t a[32];
+          const uint32_t ta = tmem + tlane + 32 * j;   // columns 0..319: O^T then l
+          tmem_ld32(ta, a);
+          const float4* al4 = reinterpret_cast<const float4*>(s_alpha + 32 * (j & 1));
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = al4[q];
+            a[4 * q] = __float_as_uint(__uint_as_float(a[4 * q]) * f.x);
+            a[4 * q + 1] = __float_as_uint(__uint_as_float(a[4 * q + 1]) * f.y);
+            a[4 * q + 2] = __float_as_uint(__uint_as_float(a[4 * q + 2]) * f.z);
+            a[4 * q + 3] = __float_as_uint(__uint_as_float(a[4 * q + 3]) * f.w);
+          }
+          tmem_st32(ta, a);
+        }
+        tc_wait_st();
+      }
+      if (tt == T - 1 && r < 64) reinterpret_cast<float*>(c.sm + SM_MFIN)[64 * b + r] = s_m[r];
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(c, B_PFULL));
+      if (tt == T - 1) mbar_arrive(bar(c, B_MFIN));   // the item's final reference max
+      ++g;
+      if (tt + 1 < T) {
+        sm_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, g);
+        if (c.misc[M_ABORT]) return;
       }
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
+    ++seq;
+    if (open_item() <= 0) return;
   }
 }
 
-// ================================================================== VD
-// Eight lanes per row read 128 contiguous bytes (one d-tile of the latent) and write the
-// fp16 values straight into the MN-major V~ block; no thread-per-row mapping is needed.
-DSA_DEV void vd_role(const KParams& P, const Ctx& c, int w, int lane) {
-  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  float* s_sc = reinterpret_cast<float*>(c.sm + SM_VDSC + w * 512);   // [32 rows][4 scales]
-  const int sub = lane >> 3, ch = lane & 7;
-  uint32_t vq = 0;
-  for (uint32_t seq = 0;; ++seq) {
-    const int b = seq & 1;
-    const int* info = s_items + 8 * b;
-    if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
-    if (info[IT_ITEM] < 0) return;
-    const int T = info[IT_T], row0 = info[IT_ROW0], nrows = info[IT_NROWS];
-    const uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
-    for (int tt = 0; tt < T; ++tt) {
-      const int r = w * 32 + lane;
-      const bool valid = tt * TILE + r < nrows;
-      const uint32_t entry = valid ? __ldg(list + row0 + tt * TILE + r) : 0u;
-      {
-        const uint4 sc = valid ? ldg_nc(row_ptr(P, entry) + D_LAT) : make_uint4(0, 0, 0, 0);
-        __syncwarp();                                   // previous tile's scales consumed
-        *reinterpret_cast<uint4*>(s_sc + 4 * lane) = sc;
-        __syncwarp();
-      }
-      const uint8_t* src[8];
-      bool sv[8];
+// ================================================================== EPI
+// 1/rms of every head of q[t] (fp32 statistics) times softmax_scale * log2(e): eight
+// lanes per head, sixteen heads per pass of the 128 threads.
+DSA_DEV void q_stats(const KParams& P, const Ctx& c, int b, int er, Group& grp) {
+  const int t = item_info(c, b)[IT_TOKEN];
+  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
+  const int hs = er >> 3, sl = er & 7;
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    uint4 raw[1][9];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t e = __shfl_sync(0xFFFFFFFFu, entry, 4 * k + sub);
-        sv[k] = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, 4 * k + sub) != 0;
-        src[k] = row_ptr(P, e) + 16 * ch;
-      }
-      uint4 L[2][8];
+    for (int u = 0; u < 1; ++u) {
+      const int h = 16 * (it + u) + hs;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) L[0][k] = sv[k] ? ldg_nc(src[k]) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j < 3) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) L[(j + 1) & 1][k] = sv[k] ? ldg_nc(src[k] + 128 * (j + 1)) : make_uint4(0, 0, 0, 0);
-        }
-        const uint32_t slot = vq % V_SLOTS;
-        if (!wait_bar_w(c, B_VEMPTY + slot, ((vq / V_SLOTS) & 1) ^ 1)) return;
-        const uint32_t base = c.sb + SM_V + slot * 32768 + (uint32_t)(ch >> 2) * 16384;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t row = (uint32_t)(w * 32 + 4 * k + sub);
-          const __half2 s2 = __float2half2_rn(s_sc[4 * (4 * k + sub) + j]);
-          uint32_t v[8];
-          dequant16(L[j & 1][k], s2, v);
-          // dims [16 ch, 16 ch + 16) of the d-tile = 8-dim chunks 2(ch % 4), +1 of atom ch / 4
-          const uint32_t rsw = row & 7;
-          const uint32_t rb = base + (row >> 3) * 1024 + rsw * 128;
-          const uint32_t c0 = (uint32_t)(2 * (ch & 3));
-          sts128(rb + ((c0 ^ rsw) << 4), make_uint4(v[0], v[1], v[2], v[3]));
-          sts128(rb + (((c0 + 1) ^ rsw) << 4), make_uint4(v[4], v[5], v[6], v[7]));
-        }
-        fence_async_smem();
-        mbar_arrive(bar(c, B_VFULL + slot));
-        ++vq;
-      }
+      for (int k = 0; k < 9; ++k)
+        raw[u][k] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + (sl + 8 * k) * 8)
+                                : make_uint4(0, 0, 0, 0);
     }
-    mbar_arrive(bar(c, B_ITEMPTY + b));
+#pragma unroll
+    for (int u = 0; u < 1; ++u) {
+      const int h = 16 * (it + u) + hs;
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 9; ++k) {
+        const uint32_t w4[4] = {raw[u][k].x, raw[u][k].y, raw[u][k].z, raw[u][k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(w4[e] << 16), bb = __uint_as_float(w4[e] & 0xFFFF0000u);
+          ss = fmaf(a, a, fmaf(bb, bb, ss));
+        }
+      }
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
+      if (sl == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(ss * (1.0f / D_QK) + P.rms_eps) * P.score_scale_log2 : 0.f;
+    }
   }
+  grp.sync(c);
 }
 
-// ================================================================== SM + epilogue
-// Finish 32 consecutive output dims of one head: inverse RoPE, optional pre-cast store,
-// MXFP8 (one 32-value block) and the stores.
+// q~ of one item: 64 heads x 9 atoms x 8 chunks of 8 dims; thread-piece p covers head
+// (p / 8) % 64, chunk p % 8, atom p / 512, so one warp reads four 128-byte head rows and
+// writes them with conflict-free swizzled stores.
+DSA_DEV void build_q(const KParams& P, const Ctx& c, int b, int er) {
+  const int* info = item_info(c, b);
+  const int t = info[IT_TOKEN];
+  const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
+  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  const uint16_t* s_w = reinterpret_cast<const uint16_t*>(c.sm + SM_NORMW);
+#pragma unroll 1
+  for (int j0 = 0; j0 < 36; j0 += 9) {
+    uint4 raw[9];
+#pragma unroll
+    for (int u = 0; u < 9; ++u) {
+      const int p = er + 128 * (j0 + u);
+      const int a = p >> 9, h = (p >> 3) & 63, chn = p & 7;
+      raw[u] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + 64 * a + 8 * chn)
+                           : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 9; ++u) {
+      const int p = er + 128 * (j0 + u);
+      const int a = p >> 9, h = (p >> 3) & 63, chn = p & 7;
+      const int d0 = 64 * a + 8 * chn;
+      const float inv = s_inv[h];
+      const uint4 wv = *reinterpret_cast<const uint4*>(s_w + d0);
+      const uint32_t x4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+      const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(x4[e] << 16) * inv * __uint_as_float(w4[e] << 16);
+        x[2 * e + 1] = __uint_as_float(x4[e] & 0xFFFF0000u) * inv * __uint_as_float(w4[e] & 0xFFFF0000u);
+      }
+      if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 cs = rope[4 * chn + e];
+          const float x0 = x[2 * e], x1 = x[2 * e + 1];
+          x[2 * e] = x0 * cs.x - x1 * cs.y;
+          x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+        }
+      }
+      const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                 pack_f16x2(x[6], x[7]));
+      sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
+    }
+  }
+  fence_async_smem();
+}
+
+// Finish 32 consecutive output dims of one head in one thread: inverse RoPE, optional
+// pre-cast store, MXFP8 (one 32-value block) and the stores.
 DSA_DEV void finalize_block(const KParams& P, float (&v)[32], int t, int h, int d0, const float2* rope) {
   if (d0 >= 448) {
 #pragma unroll
@@ -618,283 +778,243 @@ DSA_DEV void finalize_block(const KParams& P, float (&v)[32], int t, int h, int 
   P.out_sf[row * 16 + (d0 >> 5)] = (uint8_t)(E + 127);
 }
 
-DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
-  const int r = q4 * 32 + lane;
-  const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
-  const int* s_items = reinterpret_cast<const int*>(c.sm + SM_ITEM);
-  float* s_mref = reinterpret_cast<float*>(c.sm + SM_MREF);
-  float* s_lacc = reinterpret_cast<float*>(c.sm + SM_LACC);
-  float* s_alpha = reinterpret_cast<float*>(c.sm + SM_ALPHA);
-  float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
-  float* s_lpart = reinterpret_cast<float*>(c.sm + SM_LPART);
-  float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);
-  float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
-  // this warp's epilogue slab: 64 rows (heads) of 32 fp32 (dims), 16-byte chunks of a row
-  // XOR-swizzled by (row & 7) so that both the column writes and the row reads are free
-  // of bank conflicts
-  uint8_t* slab = c.sm + SM_P + q4 * EPI_SLAB_BYTES;
-  const float c2 = P.score_scale_log2;
-  const float ln2 = 0.69314718055994531f;
-  uint32_t g = 0, n_grp = 0, n_ot = 0;
-  auto grp_sync = [&]() -> bool {
-    mbar_arrive(bar(c, B_GRP));
-    const bool ok = wait_bar_w(c, B_GRP, n_grp & 1);
-    ++n_grp;
-    return ok;
-  };
-  auto fold_lpart = [&](uint32_t tile) {
-    if (r < 64) {
-      const float* lp = s_lpart + 256 * (tile & 1);
-      s_lacc[r] += ((lp[r] + lp[64 + r]) + lp[128 + r]) + lp[192 + r];
+// Finish dim d of heads h0..h0+31 held one head per register (the warp holds one
+// 32-dim MXFP8 block of each head): inverse RoPE with the neighbouring lane, optional
+// pre-cast store, block amax across the warp, scale codes and E4M3 codes.  Stores of
+// one head from the 32 lanes are contiguous.
+DSA_DEV void finalize_lanes(const KParams& P, const Ctx& c, float (&v)[32], int t, int h0, int d, int e, int lane,
+                            const float2* rope) {
+  if (d >= 448) {
+    const float2 cs = rope[(d - 448) >> 1];
+    const bool odd = d & 1;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
+      // pair (x0, x1) rotated by -angle: (x0 c + x1 s, -x0 s + x1 c)
+      v[i] = odd ? fmaf(-o, cs.y, v[i] * cs.x) + 0.0f : fmaf(o, cs.y, v[i] * cs.x) + 0.0f;
     }
-  };
+  }
+  const size_t row0 = (size_t)t * P.h_q;
+  if (P.out_precast) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (h0 + i < P.h_q) P.out_precast[(row0 + h0 + i) * D_LAT + d] = v[i];
+  }
+  float am[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am[i] = fabsf(v[i]);
+  reduce32<true>(am, lane);           // lane L: amax of head h0 + L
+  int E = (int)((__float_as_uint(am[0]) >> 23) & 0xFF) - 127 - 8;
+  E = E < -127 ? -127 : E;
+  float* s_scl = reinterpret_cast<float*>(c.sm + SM_ESCL) + 32 * e;
+  s_scl[lane] = __uint_as_float((uint32_t)(127 - E) << 23);
+  if (h0 + lane < P.h_q) P.out_sf[(row0 + h0 + lane) * 16 + (d >> 5)] = (uint8_t)(E + 127);
+  __syncwarp();
+  const float4* s4 = reinterpret_cast<const float4*>(s_scl);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 f = s4[q];
+    const uint32_t lo = f32x2_to_e4m3x2(v[4 * q] * f.x, v[4 * q + 1] * f.y);
+    const uint32_t hi = f32x2_to_e4m3x2(v[4 * q + 2] * f.z, v[4 * q + 3] * f.w);
+    const uint8_t b4[4] = {(uint8_t)lo, (uint8_t)(lo >> 8), (uint8_t)hi, (uint8_t)(hi >> 8)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (h0 + 4 * q + k < P.h_q) P.out_fp8[(row0 + h0 + 4 * q + k) * D_LAT + d] = b4[k];
+  }
+  __syncwarp();
+}
+
+DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int lane) {
+  const int er = e * 32 + lane;
+  const uint32_t tlane = (uint32_t)(e * 32) << 16;
+  float* s_el = reinterpret_cast<float*>(c.sm + SM_EL);
+  float* s_else = reinterpret_cast<float*>(c.sm + SM_ELSE);
+  const float ln2 = 0.69314718055994531f;
+  const bool is_split = P.n_splits > 1;
+  Group grp{B_EPG, 0};
+  uint32_t nq = 0;
+  int built = -1;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq & 1;
-    const int* info = s_items + 8 * b;
     if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
+    const int* info = item_info(c, b);
     if (info[IT_ITEM] < 0) return;
-    const int t = info[IT_TOKEN], split = info[IT_SPLIT], T = info[IT_T], nrows = info[IT_NROWS];
+    const int t = info[IT_TOKEN], split = info[IT_SPLIT], T = info[IT_T];
     const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-    if (r < 64) {
-      s_mref[r] = -INFINITY;
-      s_lacc[r] = 0.f;
-    }
-    if (!grp_sync()) return;
-
-    for (int tt = 0; tt < T; ++tt) {
-      const uint32_t sb = g & 1;
-      const uint32_t ts = tmem + tlane + TM_S + 64 * sb;
-      const bool valid = r < nrows - tt * TILE;
-      if (!wait_bar_w(c, B_SFULL + sb, (g >> 1) & 1)) return;
+    if (T > 0) {
+      if (built != (int)seq) {
+        q_stats(P, c, b, er, grp);
+        if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return;
+        build_q(P, c, b, er);
+        mbar_arrive(bar(c, B_QREADY));
+      }
+      // build the next item's q~ as soon as this item's QK^T no longer reads it
+      {
+        const int nb = b ^ 1;
+        if (!wait_bar_w(c, B_ITFULL + nb, ((seq + 1) >> 1) & 1)) return;
+        const int* ninfo = item_info(c, nb);
+        if (ninfo[IT_ITEM] >= 0 && ninfo[IT_T] > 0) {
+          q_stats(P, c, nb, er, grp);
+          if (!wait_bar_w(c, B_QFREE, nq & 1)) return;
+          build_q(P, c, nb, er);
+          mbar_arrive(bar(c, B_QREADY));
+          built = (int)seq + 1;
+        }
+      }
+      if (!wait_bar_w(c, B_ODONE, nq & 1)) return;
+      if (!wait_bar_w(c, B_MFIN, nq & 1)) return;
       tc_fence_after();
-      // pass 1: how far does this tile exceed the reference max of each head?
-      float dmax = -INFINITY;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      // row sums (every TMEM lane holds all 64) -> 1/l and the LSE
+      if (e == 0) {
         uint32_t a[32];
-        tmem_ld32(ts + 32 * half, a);
-        tc_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = valid ? __uint_as_float(a[i]) * c2 : -INFINITY;
-          dmax = fmaxf(dmax, x - s_mref[32 * half + i]);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xFFFFFFFFu, dmax, o));
-      if (lane == 0) s_flag[4 * (g & 1) + q4] = dmax;
-      if (!grp_sync()) return;
-      if (tt > 0) fold_lpart(g - 1);
-      const float* fl = s_flag + 4 * (g & 1);
-      const float need_v = fmaxf(fmaxf(fl[0], fl[1]), fmaxf(fl[2], fl[3]));
-      const bool need = !(need_v <= 8.0f);
-      if (need) {
-        // exact tile max per head, new reference max, rescale factors
-#pragma unroll
-        for (int hb = 0; hb < 4; ++hb) {
-          uint32_t a[16];
-          tmem_ld16(ts + 16 * hb, a);
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_ld32(tmem + tlane + TM_L + 32 * hf, a);
           tc_wait_ld();
-          float v[16];
+          if (lane == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = valid ? __uint_as_float(a[i]) * c2 : -INFINITY;
-          reduce16<true>(v, lane);
-          s_red[q4 * 64 + 16 * hb + (lane >> 1)] = v[0];
-        }
-        if (!grp_sync()) return;
-        if (r < 64) {
-          const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
-          const float mo = s_mref[r];
-          const float mn = fmaxf(mo, tm);
-          const float al = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-          s_mref[r] = mn;
-          s_alpha[r] = al;
-          s_lacc[r] *= al;
-        }
-        if (!grp_sync()) return;
-      }
-      // P buffer g & 1 is free once the PV two tiles back has completed
-      const uint32_t pb = g & 1;
-      if (!wait_bar_w(c, B_PEMPTY + pb, ((g >> 1) & 1) ^ 1)) return;
-      // pass 2: P = exp2(x - m) in fp16, row r of the MN-major B operand; row sums
-      const uint32_t prow = c.sb + SM_P + pb * 16384 + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32];
-        tmem_ld32(ts + 32 * half, a);
-        tc_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = valid ? __uint_as_float(a[2 * i]) * c2 : -INFINITY;
-          const float x1 = valid ? __uint_as_float(a[2 * i + 1]) * c2 : -INFINITY;
-          pk[i] = pack_f16x2(exp2f(x0 - s_mref[32 * half + 2 * i]), exp2f(x1 - s_mref[32 * half + 2 * i + 1]));
-        }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint32_t chunk = (uint32_t)(4 * half + cc);
-          sts128(prow + ((chunk ^ (uint32_t)(r & 7)) << 4),
-                 make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]));
-        }
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[2 * i] = f16lo(pk[8 * hb + i]);
-            v[2 * i + 1] = f16hi(pk[8 * hb + i]);
+            for (int i = 0; i < 32; ++i) s_el[32 * hf + i] = __uint_as_float(a[i]);
           }
-          reduce16<false>(v, lane);
-          if ((lane & 1) == 0) s_lpart[256 * (g & 1) + 64 * q4 + 32 * half + 16 * hb + (lane >> 1)] = v[0];
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(c, B_SEMPTY + sb));     // S^T fully read
-      if (need && tt > 0) {
-        // O^T is rescaled once the PV of the previous tile has completed
-        if (!wait_bar_w(c, B_PEMPTY + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
-        tc_fence_after();
+      if (!grp.sync(c)) return;
+      if (er < 64) {
+        const float l = s_el[er];
+        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[64 * b + er];
+        const bool any = l > 0.f;
+        s_else[er] = any ? mfin + log2f(l) : -INFINITY;
+        s_el[er] = any ? 1.f / l : 0.f;
+      }
+      if (!grp.sync(c)) return;
+      if (!is_split && P.out_lse && er < P.h_q) P.out_lse[(size_t)t * P.h_q + er] = s_else[er] * ln2;
+      if (is_split && er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = s_else[er];
 #pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
+      for (int cidx = 0; cidx < 4; ++cidx) {
+        const int d = 128 * cidx + 32 * e + lane;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
           uint32_t a[32];
-          const uint32_t ta = tmem + tlane + TM_O + 32 * j;
-          tmem_ld32(ta, a);
+          tmem_ld32(tmem + tlane + TM_O + 64 * cidx + 32 * hf, a);
           tc_wait_ld();
-          const float* al = s_alpha + 32 * (j & 1);
+          if (hf == 1) {
+            tc_fence_before();
+            mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
+          }
+          float v[32];
+          const float4* il4 = reinterpret_cast<const float4*>(s_el + 32 * hf);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(__uint_as_float(a[i]) * al[i]);
-          tmem_st32(ta, a);
-        }
-        tc_wait_st();
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(c, B_PFULL + pb));
-      ++g;
-    }
-
-    // ---------------------------------------------------------- epilogue
-    if (T > 0) {
-      if (!wait_bar_w(c, B_ODONE, n_ot & 1)) return;
-      tc_fence_after();
-    }
-    if (!grp_sync()) return;                 // last row sums written, P buffers idle
-    if (T > 0) fold_lpart(g - 1);
-    const bool is_split = P.n_splits > 1;
-    if (r < 64) {
-      const float l = s_lacc[r];
-      const bool any = T > 0 && l > 0.f;
-      s_alpha[r] = any ? 1.f / l : 0.f;
-      const float lse2 = any ? s_mref[r] + log2f(l) : -INFINITY;
-      if (is_split) P.part_lse[((size_t)t * P.n_splits + split) * HP + r] = lse2;
-      else if (P.out_lse && r < P.h_q) P.out_lse[(size_t)t * P.h_q + r] = lse2 * ln2;
-    }
-    if (!grp_sync()) return;
-    // this warp's slabs: dims [128j + 32 q4, +32) of every head
-    for (int j = 0; j < 4; ++j) {
-      const int d0 = 128 * j + 32 * q4;
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = il4[q];
+            v[4 * q] = __uint_as_float(a[4 * q]) * f.x;
+            v[4 * q + 1] = __uint_as_float(a[4 * q + 1]) * f.y;
+            v[4 * q + 2] = __uint_as_float(a[4 * q + 2]) * f.z;
+            v[4 * q + 3] = __uint_as_float(a[4 * q + 3]) * f.w;
+          }
+          if (is_split) {
+            float* dst = P.part_o + (((size_t)t * P.n_splits + split) * HP + 32 * hf) * D_LAT + d;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32];
-        if (T > 0) {
-          tmem_ld32(tmem + tlane + TM_O + 64 * j + 32 * half, a);
-          tc_wait_ld();
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = 32 * half + i;
-          const float v = (T > 0) ? __uint_as_float(a[i]) * s_alpha[h] : 0.f;
-          const uint32_t off = (uint32_t)h * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(h & 7)) << 4) + (lane & 3) * 4;
-          *reinterpret_cast<float*>(slab + off) = v;
+            for (int i = 0; i < 32; ++i) dst[(size_t)i * D_LAT] = v[i];
+          } else {
+            finalize_lanes(P, c, v, t, 32 * hf, d, e, lane, rope);
+          }
         }
       }
-      __syncwarp();
-#pragma unroll 1
-      for (int e = 0; e < 2; ++e) {
-        const int h = lane + 32 * e;
-        float v[32];
+      ++nq;
+    } else {
+      // no valid column: o = 0, scale codes 0, LSE -inf
+      if (is_split) {
+        if (er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = -INFINITY;
+      } else {
+        for (int i = er; i < P.h_q * 32; i += N_EPI) {
+          const int h = i >> 5, k = i & 31;
+          reinterpret_cast<uint4*>(P.out_fp8 + ((size_t)t * P.h_q + h) * D_LAT)[k] = make_uint4(0, 0, 0, 0);
+          if (P.out_precast) {
+            float4* pc = reinterpret_cast<float4*>(P.out_precast + ((size_t)t * P.h_q + h) * D_LAT);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 f = *reinterpret_cast<const float4*>(slab + h * 128 + ((k ^ (h & 7)) << 4));
-          v[4 * k] = f.x;
-          v[4 * k + 1] = f.y;
-          v[4 * k + 2] = f.z;
-          v[4 * k + 3] = f.w;
+            for (int u = 0; u < 4; ++u) pc[4 * k + u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        if (is_split) {
-          float4* dst = reinterpret_cast<float4*>(P.part_o + (((size_t)t * P.n_splits + split) * HP + h) * D_LAT + d0);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        } else if (h < P.h_q) {
-          finalize_block(P, v, t, h, d0, rope);
-        }
+        for (int i = er; i < P.h_q * 16; i += N_EPI) P.out_sf[(size_t)t * P.h_q * 16 + i] = 0;
+        if (P.out_lse && er < P.h_q) P.out_lse[(size_t)t * P.h_q + er] = -INFINITY;
       }
-      __syncwarp();
-    }
-    if (T > 0) {
-      tc_fence_before();
-      mbar_arrive(bar(c, B_OFREE));          // O^T has been read
-      ++n_ot;
     }
     if (is_split) {
-      // the last split of the token to arrive combines all partials
+      // the last split of the token to arrive combines all partials after the CTA's roles
+      // have finished (one item per CTA on this path)
       __threadfence();
-      if (!grp_sync()) return;
-      if (r == 0) {
+      if (!grp.sync(c)) return;
+      if (er == 0) {
         const uint32_t old = atomicAdd(&P.counters[t], 1u);
         const int last = (old == (uint32_t)(P.n_splits - 1));
         if (last) P.counters[t] = 0u;
         c.misc[M_LAST] = last;
+        c.misc[M_TOKEN] = t;
       }
-      if (!grp_sync()) return;
-      if (c.misc[M_LAST]) {
-        __threadfence();
-        if (r < 64) {
-          const float* pl = P.part_lse + (size_t)t * P.n_splits * HP + r;
-          float M = -INFINITY;
-          for (int s = 0; s < P.n_splits; ++s) M = fmaxf(M, __ldcg(pl + s * HP));
-          float den = 0.f;
-          for (int s = 0; s < P.n_splits; ++s) {
-            const float w = (M == -INFINITY) ? 0.f : exp2f(__ldcg(pl + s * HP) - M);
-            s_cw[s * 64 + r] = w;
-            den += w;
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          for (int s = 0; s < P.n_splits; ++s) s_cw[s * 64 + r] *= inv;
-          if (P.out_lse && r < P.h_q) P.out_lse[(size_t)t * P.h_q + r] = den > 0.f ? (M + log2f(den)) * ln2 : -INFINITY;
-        }
-        if (!grp_sync()) return;
-        for (int j = 0; j < 4; ++j) {
-          const int d0 = 128 * j + 32 * q4;
-#pragma unroll 1
-          for (int e = 0; e < 2; ++e) {
-            const int h = lane + 32 * e;
-            if (h >= P.h_q) continue;
-            float v[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = 0.f;
-#pragma unroll 2
-            for (int s = 0; s < P.n_splits; ++s) {
-              const float w = s_cw[s * 64 + h];
-              if (w == 0.f) continue;
-              const float4* src =
-                  reinterpret_cast<const float4*>(P.part_o + (((size_t)t * P.n_splits + s) * HP + h) * D_LAT + d0);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float4 f = __ldcg(src + k);
-                v[4 * k] = fmaf(w, f.x, v[4 * k]);
-                v[4 * k + 1] = fmaf(w, f.y, v[4 * k + 1]);
-                v[4 * k + 2] = fmaf(w, f.z, v[4 * k + 2]);
-                v[4 * k + 3] = fmaf(w, f.w, v[4 * k + 3]);
-              }
-            }
-            finalize_block(P, v, t, h, d0, rope);
-          }
-        }
-      }
-      if (!grp_sync()) return;               // combine weights no longer needed
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
+  }
+}
+
+// Combine of one token's split partials by the whole CTA: thread = (head, 32-dim block),
+// weights exp2(lse_s - M) / sum over splits.
+DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int tid) {
+  float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);       // [MAX_SPLITS][64]
+  float* s_lse = s_cw + MAX_SPLITS * 64;                       // [64]
+  float2* s_rope = reinterpret_cast<float2*>(s_lse + 64);      // [32] (cos, sin)
+  const int ns = P.n_splits;
+  const float ln2 = 0.69314718055994531f;
+  if (tid < 64) {
+    const float* pl = P.part_lse + (size_t)t * ns * HP + tid;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(pl + s * HP));
+    float den = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float w = (M == -INFINITY) ? 0.f : exp2f(__ldcg(pl + s * HP) - M);
+      s_cw[s * 64 + tid] = w;
+      den += w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int s = 0; s < ns; ++s) s_cw[s * 64 + tid] *= inv;
+    s_lse[tid] = den > 0.f ? (M + log2f(den)) * ln2 : -INFINITY;
+  }
+  __syncthreads();
+  if (P.out_lse && tid < P.h_q) P.out_lse[(size_t)t * P.h_q + tid] = s_lse[tid];
+  // the rotary table of this token, rebuilt (the item buffers are gone)
+  if (tid < 32) {
+    const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[tid];
+    const float frac = (float)(turns >> 40) * 5.9604644775390625e-08f;
+    float sn, cs;
+    sincospif(2.0f * frac, &sn, &cs);
+    s_rope[tid] = make_float2(cs, sn);
+  }
+  __syncthreads();
+  const float2* rope = s_rope;
+  for (int u = tid; u < P.h_q * 16; u += NTHREADS) {
+    const int h = u >> 4, blk = u & 15;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = 0.f;
+    const float* base = P.part_o + ((size_t)t * ns * HP + h) * D_LAT + 32 * blk;
+#pragma unroll 1
+    for (int s = 0; s < ns; s += 2) {
+      const float w0 = s_cw[s * 64 + h];
+      const float w1 = (s + 1 < ns) ? s_cw[(s + 1) * 64 + h] : 0.f;
+      float4 f0[8], f1[8];
+      const float4* src0 = reinterpret_cast<const float4*>(base + (size_t)s * HP * D_LAT);
+      const float4* src1 = reinterpret_cast<const float4*>(base + (size_t)(s + 1) * HP * D_LAT);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f0[k] = w0 != 0.f ? __ldcg(src0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f1[k] = w1 != 0.f ? __ldcg(src1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[4 * k] = fmaf(w0, f0[k].x, fmaf(w1, f1[k].x, v[4 * k]));
+        v[4 * k + 1] = fmaf(w0, f0[k].y, fmaf(w1, f1[k].y, v[4 * k + 1]));
+        v[4 * k + 2] = fmaf(w0, f0[k].z, fmaf(w1, f1[k].z, v[4 * k + 2]));
+        v[4 * k + 3] = fmaf(w0, f0[k].w, fmaf(w1, f1[k].w, v[4 * k + 3]));
+      }
+    }
+    finalize_block(P, v, t, h, 32 * blk, rope);
   }
 }
 
@@ -912,57 +1032,60 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int i = 0; i < K_SLOTS; ++i) {
-      mbar_init(bar(c, B_KFULL + i), 128);
-      mbar_init(bar(c, B_KEMPTY + i), 1);
-    }
-    for (int i = 0; i < V_SLOTS; ++i) {
-      mbar_init(bar(c, B_VFULL + i), 128);
-      mbar_init(bar(c, B_VEMPTY + i), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(c, B_VFULL + i), N_DQ);
+      mbar_init(bar(c, B_VFREE + i), 1);
+      mbar_init(bar(c, B_OFREE + i), N_EPI);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(c, B_KRFULL + i), N_SM);
+      mbar_init(bar(c, B_KRFREE + i), 1);
       mbar_init(bar(c, B_SFULL + i), 1);
-      mbar_init(bar(c, B_SEMPTY + i), 128);
-      mbar_init(bar(c, B_PFULL + i), 128);
-      mbar_init(bar(c, B_PEMPTY + i), 1);
+      mbar_init(bar(c, B_SFREE + i), N_SM);
       mbar_init(bar(c, B_ITFULL + i), N_PREP);
-      mbar_init(bar(c, B_ITEMPTY + i), 128 + 128 + 128 + 1 + 1);   // KD, VD, SM, QK, PV
+      mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SM + N_EPI + 1);
     }
+    mbar_init(bar(c, B_PFULL), N_SM);
+    mbar_init(bar(c, B_PFREE), 1);
     mbar_init(bar(c, B_ODONE), 1);
-    mbar_init(bar(c, B_OFREE), 128);
-    mbar_init(bar(c, B_QREADY), N_PREP);
+    mbar_init(bar(c, B_QREADY), N_EPI);
     mbar_init(bar(c, B_QFREE), 1);
-    mbar_init(bar(c, B_GRP), 128);
-    mbar_init(bar(c, B_PREP), N_PREP);
-    mbar_init(bar(c, B_DRAIN), 2);
+    mbar_init(bar(c, B_MFIN), N_SM);
+    mbar_init(bar(c, B_SMG), N_SM);
+    mbar_init(bar(c, B_EPG), N_EPI);
+    mbar_init(bar(c, B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
+    c.misc[M_LAST] = 0;
   }
-  if (warp == W_QK) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
-  float* s_normw = reinterpret_cast<float*>(c.sm + SM_NORMW);
-  for (int i = tid; i < D_QK; i += NTHREADS) s_normw[i] = __uint_as_float((uint32_t)P.norm_w[i] << 16);
+  if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
+  {
+    uint16_t* s_w = reinterpret_cast<uint16_t*>(c.sm + SM_NORMW);
+    for (int i = tid; i < D_QK; i += NTHREADS) s_w[i] = P.norm_w[i];
+    uint32_t* ones = reinterpret_cast<uint32_t*>(c.sm + SM_ONES);
+    for (int i = tid; i < 1024; i += NTHREADS) ones[i] = 0x3C003C00u;   // fp16 1.0 pairs
+    fence_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)c.misc[M_TMEM];
 
-  if (warp == W_PV) {
-    if (lane == 0) pv_role(P, c, tmem);
-  } else if (warp >= W_PREP) {
-    prep_role(P, c, warp - W_PREP, lane);
-  } else if (warp == W_QK) {
-    if (lane == 0) qk_role(P, c, tmem);
-  } else if (warp >= W_SM) {
+  if (warp < W_SM) {
+    dq_role(P, c, warp, lane);
+  } else if (warp < W_EPI) {
     sm_role(P, c, tmem, warp - W_SM, lane);
-  } else if (warp >= W_KD) {
-    kd_role(P, c, tmem, warp - W_KD, lane);
+  } else if (warp < W_MMA) {
+    epi_role(P, c, tmem, warp - W_EPI, lane);
+  } else if (warp == W_MMA) {
+    if (lane == 0) mma_role(P, c, tmem);
   } else {
-    vd_role(P, c, warp - W_VD, lane);
+    prep_role(P, c, lane);
   }
 
   tc_fence_before();
   __syncthreads();
-  if ((warp == W_QK || warp == W_PV) && lane == 0) {
+  if (warp == W_MMA && lane == 0) {
     // every MMA this CTA issued has completed before TMEM is released
     tc_commit(bar(c, B_DRAIN));
     const unsigned long long start = clock64();
@@ -971,9 +1094,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == W_QK) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
+  }
+  if (P.n_splits > 1 && c.misc[M_LAST] && !c.misc[M_ABORT]) {
+    __threadfence();
+    combine_token(P, c, c.misc[M_TOKEN], tid);
   }
 }
 

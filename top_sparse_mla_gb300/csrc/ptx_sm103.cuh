@@ -81,6 +81,16 @@ DSA_DEV uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   d |= (uint64_t)2 << 61;   // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor without swizzle (8-row x 16-byte core matrices): lbo =
+// stride between core matrices along K, sbo = stride between 8-row groups.
+DSA_DEV uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 accumulate, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, uint32_t a_mn, uint32_t b_mn) {
   return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
