@@ -93,8 +93,9 @@ int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32
 
 /* Bytes of device workspace the forward call needs for `p` on a GPU with `num_sms`
  * SMs (num_sms <= 0: the current device).  The workspace holds a status word, one
- * combine counter per token and, when a token's rows are split across several CTAs,
- * the per-split partial outputs.  0 is returned for invalid parameters. */
+ * combine counter per token, the compacted row lists of every CTA and, when a token's
+ * rows are split across several CTAs, the per-split partial outputs.  0 is returned
+ * for invalid parameters. */
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
 
 /* The fused forward pass (steps 1-7). */

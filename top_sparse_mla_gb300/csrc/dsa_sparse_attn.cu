@@ -9,17 +9,20 @@
 //   DQ   (warps 0-7)   gathered rows -> fp16 latent tile [128 rows x 512 dims] in shared
 //                      memory, fp32 block scale folded in.  The one tile is the A operand
 //                      of both contractions: K-major for QK^T (M = rows), MN-major for PV
-//                      (M = dims).  The next tile's raw bytes wait in registers.
-//   SM   (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P); the rotary part
-//                      of the next tile's keys (bf16 -> fp16) into TMEM
-//   EPI  (warps 12-15) q~ = RoPE(RMSNorm(q) * w) * scale * log2(e) in fp16 as the B
-//                      operand of QK^T (fp32 statistics), built for the next item while
-//                      the current one finishes; the epilogue: O / l, inverse RoPE, MXFP8
-//                      cast and stores, or the split partials
+//                      (M = dims).  Raw bytes are loaded two chunks ahead, rows are
+//                      prefetched into L2 one tile ahead.  Between items: the MXFP8 finish
+//                      of the previous item's output block (inverse RoPE, scales, E4M3).
+//   SM   (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P) with the per-head
+//                      factor softmax_scale * log2(e) / rms(q); the rotary part of the next
+//                      tile's keys (bf16 -> fp16) into TMEM
+//   EPI  (warps 12-15) q~ = RoPE(q * w) in fp16 as the B operand of QK^T, chunk by chunk,
+//                      built for the next item while the current one finishes, and the
+//                      fp32 RMS statistics of q; the epilogue: O^T / l out of TMEM into a
+//                      global output block (or the split partial)
 //   MMA  (warp 16)     S^T[128 rows x 64 heads] = K~ . q~^T; O^T[512 x 64] += V~^T . P;
 //                      l[64] += 1^T . P (row sums on the tensor core)
-//   PREP (warp 17)     take an item, compact its valid index columns into a row list, L2
-//                      prefetch of the rows and of q, rotary table
+//   PREP (warp 17)     take an item, compact its valid index columns into a row list,
+//                      rotary table; up to three items ahead
 //
 // TMEM: O^T 0..255, l 256..319, S^T 320..447 (two buffers), K~ rope part 448..511 (two).
 // Every mbarrier wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT,
@@ -46,6 +49,7 @@ constexpr int NWARPS = 18;
 constexpr int NTHREADS = 32 * NWARPS;
 constexpr int N_DQ = 256, N_SM = 128, N_EPI = 128, N_PREP = 32;
 constexpr int MAX_SPLITS = 16;
+constexpr int NB = 4;              // item buffers: the prep warp runs up to NB - 1 items ahead
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
@@ -59,11 +63,10 @@ constexpr uint32_t SM_Q = 0;                       // q~: 9 K-atoms x [64 heads 
 constexpr uint32_t SM_V = SM_Q + 9 * 8192;         // latent tile: 4 chunks x 2 halves x 16 KB
 constexpr uint32_t SM_P = SM_V + 4 * 32768;        // P: [128 rows x 64 heads] fp16
 constexpr uint32_t SM_ONES = SM_P + 16384;         // [128 x 16] fp16 ones (A of the row sums)
-constexpr uint32_t SM_NORMW = SM_ONES + 4096;      // 576 bf16
-constexpr uint32_t SM_ROPE = SM_NORMW + 1152;      // 2 x 32 x (cos, sin)
-constexpr uint32_t SM_INV = SM_ROPE + 512;         // 2 x 64 fp32: scale * log2(e) / rms(q)
-constexpr uint32_t SM_ITEM = SM_INV + 512;         // 2 x 8 ints
-constexpr uint32_t SM_M = SM_ITEM + 64;            // 64 fp32 running max (log2 units)
+constexpr uint32_t SM_ROPE = SM_ONES + 4096;       // NB x 32 x (cos, sin)
+constexpr uint32_t SM_INV = SM_ROPE + NB * 256;    // NB x 64 fp32: softmax_scale * log2(e) / rms(q)
+constexpr uint32_t SM_ITEM = SM_INV + NB * 256;    // NB x 8 ints
+constexpr uint32_t SM_M = SM_ITEM + NB * 32;       // 64 fp32 running max (log2 units)
 constexpr uint32_t SM_ALPHA = SM_M + 256;          // 64 fp32 rescale factors
 constexpr uint32_t SM_MFIN = SM_ALPHA + 256;       // 2 x 64 fp32 final max per item
 constexpr uint32_t SM_RED = SM_MFIN + 512;         // 4 warps x 64 fp32
@@ -71,7 +74,8 @@ constexpr uint32_t SM_ESCL = SM_RED + 1024;        // 4 EPI warps x 32 fp32 bloc
 constexpr uint32_t SM_EL = SM_ESCL + 512;          // 64 fp32 row sums, then 1/l
 constexpr uint32_t SM_ELSE = SM_EL + 256;          // 64 fp32 LSE (log2 units)
 constexpr uint32_t SM_FLAG = SM_ELSE + 256;        // 2 x 4 fp32
-constexpr uint32_t SM_MISC = SM_FLAG + 32;         // misc ints
+constexpr uint32_t SM_QGEN = SM_FLAG + 32;         // NB ints: q statistics of item seq ready (seq + 1)
+constexpr uint32_t SM_MISC = SM_QGEN + 16;         // misc ints
 constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
 constexpr uint32_t SM_END = SM_BAR + 48 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
@@ -82,8 +86,8 @@ constexpr uint32_t SM_CW = SM_V;
 enum {
   B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
   B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
-  B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_ODONE = B_ITEMPTY + 2, B_OFREE,
-  B_QREADY = B_OFREE + 4, B_QFREE, B_MFIN, B_SMG, B_EPG, B_DRAIN, B_COUNT
+  B_ITFULL, B_ITEMPTY = B_ITFULL + NB, B_ODONE = B_ITEMPTY + NB, B_OFREE,
+  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_MFIN, B_SMG, B_EPG, B_DRAIN, B_COUNT
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
@@ -102,7 +106,7 @@ struct KParams {
   uint8_t* out_sf;
   float* out_precast;
   float* out_lse;
-  float* part_o;        // [s_q][n_splits][64 heads][512 dims]
+  float* part_o;        // split partials [s_q][n_splits][64 heads][512 dims]
   float* part_lse;      // [s_q][n_splits][64] (log2 units)
   uint32_t* counters;   // [s_q] split arrivals
   uint32_t* status;
@@ -138,7 +142,7 @@ DSA_DEV bool wait_bar(const Ctx& c, int b, uint32_t parity) {
   if (mbar_try(addr, parity)) return true;
   const unsigned long long start = clock64();
   while (true) {
-    if (mbar_try(addr, parity)) return true;
+    if (mbar_wait_susp(addr, parity)) return true;
     if (c.misc[M_ABORT]) return false;
     if (clock64() - start > WAIT_LIMIT_CYCLES) {
       atomicOr(c.status, DSA_STATUS_WAIT_TIMEOUT);
@@ -171,7 +175,7 @@ DSA_DEV const uint8_t* row_ptr(const KParams& P, uint32_t e) {
   return base + (size_t)(e & 0x7FFFFFFFu) * ROW_BYTES;
 }
 DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
-  return P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
+  return P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
 }
 DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 8 * b; }
 
@@ -197,19 +201,25 @@ DSA_DEV void reduce32(float (&v)[32], int lane) {
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
   const bool split_path = P.n_splits > 1;
-  for (uint32_t seq = 0;; ++seq) {
-    const int b = seq & 1;
-    int* info = s_items + 8 * b;
-    if (!wait_bar_w(c, B_ITEMPTY + b, ((seq >> 1) & 1) ^ 1)) return;
+  // split path: exactly one item per CTA (the grid has one CTA per item), so the last
+  // split of a token can run its combine with the whole CTA afterwards.  Otherwise items
+  // come from the global queue, each fetched one iteration before it is used.
+  auto fetch = [&](uint32_t seq) -> int {
     int item = 0;
     if (lane == 0) {
-      // split path: exactly one item per CTA (the grid has one CTA per item), so the
-      // last split of a token can run its combine with the whole CTA afterwards
       if (split_path) item = seq == 0 ? (int)blockIdx.x : P.n_items;
       else item = (int)atomicAdd(P.work, 1u);
       item = item < P.n_items ? item : -1;
     }
-    item = __shfl_sync(0xFFFFFFFFu, item, 0);
+    return item;
+  };
+  int next = fetch(0);
+  for (uint32_t seq = 0;; ++seq) {
+    const int b = seq % NB;
+    int* info = s_items + 8 * b;
+    if (!wait_bar_w(c, B_ITEMPTY + b, ((seq / NB) & 1) ^ 1)) return;
+    const int item = __shfl_sync(0xFFFFFFFFu, next, 0);
+    if (item >= 0) next = fetch(seq + 1);
     if (item < 0) {
       if (lane == 0) info[IT_ITEM] = -1;
       mbar_arrive(bar(c, B_ITFULL + b));   // tells every role to stop
@@ -226,29 +236,21 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       sincospif(2.0f * frac, &sn, &cs);
       rope[lane] = make_float2(cs, sn);
     }
-    // q[t] is read twice soon after (statistics, then q~)
-    if (lane < 8) {
-      const uint32_t bytes = (uint32_t)(P.h_q * D_QK * 2);
-      const uint32_t part = ((bytes / 8) + 15) & ~15u;
-      const uint32_t off = part * (uint32_t)lane;
-      if (off < bytes) prefetch_l2(reinterpret_cast<const uint8_t*>(P.q + (size_t)t * P.h_q * D_QK) + off,
-                                   off + part <= bytes ? part : bytes - off);
-    }
-    // compact the valid columns (j < topk_length, index >= 0), 256 indices per load batch
-    uint32_t* list = P.lists + ((size_t)blockIdx.x * 2 + b) * DSA_MAX_TOPK;
+    // compact the valid columns (j < topk_length, index >= 0), 512 indices per load batch
+    uint32_t* list = P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
     int L = P.topk_length[t];
     L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
     const int32_t* irow = P.indices + (size_t)t * P.topk;
     int count = 0;
-    for (int base = 0; base < L; base += 256) {
-      int v[8];
+    for (int base = 0; base < L; base += 512) {
+      int v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const int j = base + 32 * k + lane;
         v[k] = (j < L) ? __ldg(irow + j) : -1;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const int j = base + 32 * k + lane;
         const bool cmp = j >= P.n_swa_cols;
         bool valid = v[k] >= 0;
@@ -260,7 +262,10 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
           }
         }
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid);
-        if (valid) list[count + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
+        if (valid) {
+          const uint32_t e = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
+          list[count + __popc(bal & ((1u << lane) - 1u))] = e;
+        }
         count += __popc(bal);
       }
     }
@@ -273,7 +278,6 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     const int row0 = tile0 * TILE;
     const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
     __syncwarp();
-    for (int r = lane; r < nrows; r += 32) prefetch_l2(row_ptr(P, list[row0 + r]), ROW_BYTES);
     if (lane == 0) {
       info[IT_ITEM] = item;
       info[IT_TOKEN] = t;
@@ -284,6 +288,93 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     }
     mbar_arrive(bar(c, B_ITFULL + b));   // rows, tile range, rotary table
   }
+}
+
+// Output pointers of the MXFP8 finish (passed by value to the out-of-line callers).
+struct OutPtrs {
+  uint8_t* fp8;
+  uint8_t* sf;
+  float* precast;
+  int h_q;
+};
+
+// Finish 32 consecutive output dims of one head in one thread: inverse RoPE, optional
+// pre-cast store, MXFP8 (one 32-value block) and the stores.
+DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int d0, const float2* rope) {
+  if (d0 >= 448) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float2 cs = rope[((d0 - 448) >> 1) + k];
+      const float x0 = v[2 * k], x1 = v[2 * k + 1];
+      v[2 * k] = fmaf(x1, cs.y, x0 * cs.x) + 0.0f;     // +0.0f: a rotated exact zero stays +0
+      v[2 * k + 1] = fmaf(-x0, cs.y, x1 * cs.x) + 0.0f;
+    }
+  }
+  const size_t row = (size_t)t * O.h_q + h;
+  if (O.precast) {
+    float4* dst = reinterpret_cast<float4*>(O.precast + row * D_LAT + d0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 8;   // floor(log2 amax) - 8
+  E = E < -127 ? -127 : E;
+  const float inv = __uint_as_float((uint32_t)(127 - E) << 23);    // 2^-E, exact
+  uint32_t wq[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t lo = f32x2_to_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv);
+    const uint32_t hi = f32x2_to_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv);
+    wq[k] = lo | (hi << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(O.fp8 + row * D_LAT + d0);
+  dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+  dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+  O.sf[row * 16 + (d0 >> 5)] = (uint8_t)(E + 127);
+}
+
+// Finish dim d of heads h0..h0+15, one head per register; the 32 lanes of the warp hold
+// one 32-dim MXFP8 block of each head.  Inverse RoPE with the neighbouring lane, optional
+// pre-cast store, block amax across the warp (redux), UE8M0 code, E4M3 codes.  A head's
+// stores from the 32 lanes are contiguous.
+DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[16], int t, int h0, int d, int lane, const float2* rope) {
+  if (d >= 448) {
+    const float2 cs = rope[(d - 448) >> 1];
+    const bool odd = d & 1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
+      // pair (x0, x1) rotated by -angle: (x0 c + x1 s, -x0 s + x1 c)
+      v[i] = odd ? fmaf(-o, cs.y, v[i] * cs.x) + 0.0f : fmaf(o, cs.y, v[i] * cs.x) + 0.0f;
+    }
+  }
+  const size_t row0 = (size_t)t * O.h_q + h0;
+  if (O.precast) {
+    float* pc = O.precast + row0 * D_LAT + d;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (h0 + i < O.h_q) pc[(size_t)i * D_LAT] = v[i];
+  }
+  uint8_t* out = O.fp8 + row0 * D_LAT + d;
+  uint32_t sfw = 0;   // this lane's scale code (lane i < 16: head h0 + i)
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    float am0, am1;
+    asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(am0) : "f"(v[i]));
+    asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(am1) : "f"(v[i + 1]));
+    int e0 = (int)((__float_as_uint(am0) >> 23) & 0xFF) - 127 - 8;   // floor(log2 amax) - 8
+    int e1 = (int)((__float_as_uint(am1) >> 23) & 0xFF) - 127 - 8;
+    e0 = e0 < -127 ? -127 : e0;
+    e1 = e1 < -127 ? -127 : e1;
+    const float s0 = __uint_as_float((uint32_t)(127 - e0) << 23), s1 = __uint_as_float((uint32_t)(127 - e1) << 23);
+    const uint32_t q = f32x2_to_e4m3x2(v[i] * s0, v[i + 1] * s1);
+    if (h0 + i < O.h_q) out[(size_t)i * D_LAT] = (uint8_t)q;
+    if (h0 + i + 1 < O.h_q) out[(size_t)(i + 1) * D_LAT] = (uint8_t)(q >> 8);
+    sfw = lane == i ? (uint32_t)(e0 + 127) : (lane == i + 1 ? (uint32_t)(e1 + 127) : sfw);
+  }
+  if (lane < 16 && h0 + lane < O.h_q) O.sf[(row0 + lane) * 16 + (d >> 5)] = (uint8_t)sfw;
 }
 
 // ================================================================== DQ
@@ -334,8 +425,8 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
   // in flight
   auto open_item = [&]() -> int {   // 1 = opened, 0 = no more items, -1 = aborted
     while (true) {
-      const int b = seq & 1;
-      if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return -1;
+      const int b = seq % NB;
+      if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return -1;
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
@@ -349,16 +440,30 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
       ++seq;
     }
   };
-  if (open_item() <= 0) return;
-  while (true) {
-    const int b = seq & 1;
+  int r = open_item();
+  while (r > 0) {
+    const int b = seq % NB;
     const int* info = item_info(c, b);
     const int T = info[IT_T], nrows = info[IT_NROWS];
     const uint32_t* list = item_list(P, b) + info[IT_ROW0];
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
       const bool more = tt + 1 < T;
-      if (more) dq_load_rows(list, tt + 1, nrows, w, sub, ch, nxt);
+      // rows of the next tile (of this item, or tile 0 of the next item when its info is
+      // already out), to be prefetched into L2 one tile ahead of their loads
+      bool pf = more;
+      if (more) {
+        dq_load_rows(list, tt + 1, nrows, w, sub, ch, nxt);
+      } else {
+        const int nb = (seq + 1) % NB;
+        if (__all_sync(0xFFFFFFFFu, mbar_try(bar(c, B_ITFULL + nb), ((seq + 1) / NB) & 1))) {
+          const int* ni = item_info(c, nb);
+          if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
+            dq_load_rows(item_list(P, nb) + ni[IT_ROW0], 0, ni[IT_NROWS], w, sub, ch, nxt);
+            pf = true;
+          }
+        }
+      }
 #pragma unroll
       for (int cidx = 0; cidx < 4; ++cidx) {
         if (!wait_bar_w(c, B_VFREE + cidx, (g & 1) ^ 1)) return;
@@ -377,9 +482,18 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
         }
         fence_async_smem();
         mbar_arrive(bar(c, B_VFULL + cidx));
+        if (cidx == 0 && pf && ch < 6) {
+          // the six 128-byte lines of each next row, one line per lane
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (nxt.v[k]) prefetch_line_l2(row_ptr(P, nxt.e[k]) + 128 * ch);
+        }
         // the chunk two ahead
-        if (cidx < 2) dq_load_chunk(P, raw[cidx & 1], cidx + 2, cur, ch);
-        else if (more) dq_load_chunk(P, raw[cidx & 1], cidx - 2, nxt, ch);
+        if (cidx < 2) {
+          dq_load_chunk(P, raw[cidx & 1], cidx + 2, cur, ch);
+        } else if (more) {
+          dq_load_chunk(P, raw[cidx & 1], cidx - 2, nxt, ch);
+        }
       }
       if (more) {
         scl = dq_load_scales(P, nxt);
@@ -389,54 +503,73 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
     ++seq;
-    if (open_item() <= 0) return;
+    r = open_item();
   }
 }
 
 // ================================================================== MMA issuer
+// Descriptor plus a byte offset: the start address field holds address >> 4 in the low
+// 14 bits, and no offset used here carries out of it.
+// (an asm add, so that the compiler does not hoist every descriptor of the unrolled loops
+// into registers)
+DSA_DEV uint64_t dadd(uint64_t d, uint32_t bytes) {
+  uint32_t lo;
+  asm volatile("add.u32 %0, %1, %2;" : "=r"(lo) : "r"((uint32_t)d), "r"(bytes >> 4));
+  return ((uint64_t)(uint32_t)(d >> 32) << 32) | lo;
+}
+
 DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   constexpr uint32_t IDESC_QK = idesc_f16(128, HP, 0, 0);
   constexpr uint32_t IDESC_PV = idesc_f16(128, HP, 1, 1);
   constexpr uint32_t IDESC_L = idesc_f16(128, HP, 0, 1);
-  const uint64_t ones_desc = sdesc_noswz(c.sb + SM_ONES, 128, 256);
+  // every descriptor of the loop is one of these plus a constant offset
+  const uint64_t d_k = sdesc(c.sb + SM_V, 16, 1024);        // latent tile, K-major (QK^T)
+  const uint64_t d_v = sdesc(c.sb + SM_V, 16384, 1024);     // latent tile, MN-major (PV)
+  const uint64_t d_q = sdesc(c.sb + SM_Q, 16, 1024);        // q~
+  const uint64_t d_p = sdesc(c.sb + SM_P, 16384, 1024);     // P
+  const uint64_t d_one = sdesc_noswz(c.sb + SM_ONES, 128, 256);
   uint32_t g = 0, nq = 0;
   for (uint32_t seq = 0;; ++seq) {
-    const int b = seq & 1;
-    if (!wait_bar(c, B_ITFULL + b, (seq >> 1) & 1)) return;
+    const int b = seq % NB;
+    if (!wait_bar(c, B_ITFULL + b, (seq / NB) & 1)) return;
     const int* info = item_info(c, b);
     const int item = info[IT_ITEM];
     const int T = info[IT_T];
     mbar_arrive(bar(c, B_ITEMPTY + b));
     if (item < 0) return;
     if (T == 0) continue;
-    if (!wait_bar(c, B_QREADY, nq & 1)) return;
-    tc_fence_after();
     for (int tt = 0; tt < T; ++tt) {
       // ---- S^T = K~ . q~^T
       const uint32_t sb = g & 1;
       const uint32_t d_s = tmem + TM_S + 64 * sb;
       if (!wait_bar(c, B_SFREE + sb, ((g >> 1) & 1) ^ 1)) return;
+#pragma unroll
       for (int cidx = 0; cidx < 4; ++cidx) {
+        // q~ chunk (first tile of an item) and the latent chunk of this tile
+        if (tt == 0 && !wait_bar(c, B_QRDY + cidx, nq & 1)) return;
         if (!wait_bar(c, B_VFULL + cidx, g & 1)) return;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = SM_V + cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t boff = SM_Q + (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
-          mma_ss(d_s, sdesc(c.sb + aoff, 16, 1024), sdesc(c.sb + boff, 16, 1024), IDESC_QK, (cidx | kk) ? 1u : 0u);
+          const uint32_t aoff = cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint32_t boff = (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
+          mma_ss(d_s, dadd(d_k, aoff), dadd(d_q, boff), IDESC_QK, (cidx | kk) ? 1u : 0u);
         }
       }
+      if (tt == 0 && !wait_bar(c, B_QRDY + 4, nq & 1)) return;
       if (!wait_bar(c, B_KRFULL + sb, (g >> 1) & 1)) return;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_ts(d_s, tmem + TM_KR + 32 * sb + 8 * kk, sdesc(c.sb + SM_Q + 8 * 8192 + kk * 32, 16, 1024), IDESC_QK, 1u);
+        mma_ts(d_s, tmem + TM_KR + 32 * sb + 8 * kk, dadd(d_q, 8 * 8192 + kk * 32), IDESC_QK, 1u);
       tc_commit(bar(c, B_SFULL + sb));
       tc_commit(bar(c, B_KRFREE + sb));
       if (tt == T - 1) tc_commit(bar(c, B_QFREE));   // q~ may be rebuilt after these MMAs
       // ---- O^T += V~^T . P, l += 1^T . P
       if (!wait_bar(c, B_PFULL, g & 1)) return;
       tc_fence_after();
+      const uint32_t first = tt == 0 ? 0u : 1u;
+#pragma unroll
       for (int cidx = 0; cidx < 4; ++cidx) {
         if (tt == 0 && nq > 0) {
           // the previous item's epilogue has read this part of O^T (and l)
@@ -444,18 +577,13 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
           tc_fence_after();
         }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc(c.sb + SM_V + cidx * 32768 + kk * 2048, 16384, 1024);
-          const uint64_t bd = sdesc(c.sb + SM_P + kk * 2048, 16384, 1024);
-          mma_ss(tmem + TM_O + 64 * cidx, ad, bd, IDESC_PV, (tt == 0 && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + TM_O + 64 * cidx, dadd(d_v, cidx * 32768 + kk * 2048), dadd(d_p, kk * 2048), IDESC_PV,
+                 kk == 0 ? first : 1u);
         tc_commit(bar(c, B_VFREE + cidx));
       }
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t bd = sdesc(c.sb + SM_P + kk * 2048, 16384, 1024);
-        mma_ss(tmem + TM_L, ones_desc, bd, IDESC_L, (tt == 0 && kk == 0) ? 0u : 1u);
-      }
+      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + TM_L, d_one, dadd(d_p, kk * 2048), IDESC_L, kk == 0 ? first : 1u);
       tc_commit(bar(c, B_PFREE));
       if (tt == T - 1) tc_commit(bar(c, B_ODONE));
       ++g;
@@ -499,12 +627,12 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
   float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
   Group grp{B_SMG, 0};
-  uint32_t g = 0, seq = 0;
+  uint32_t g = 0, seq = 0, nq = 0;   // tiles, items, items with tiles
   // next item with tiles: its info waited for and the rope of its tile 0 converted
   auto open_item = [&]() -> int {
     while (true) {
-      const int b = seq & 1;
-      if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return -1;
+      const int b = seq % NB;
+      if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return -1;
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
@@ -517,10 +645,31 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   };
   if (open_item() <= 0) return;
   while (true) {
-    const int b = seq & 1;
+    const int b = seq % NB;
     const int* info = item_info(c, b);
     const int T = info[IT_T], nrows = info[IT_NROWS];
     const uint32_t* list = item_list(P, b) + info[IT_ROW0];
+    // the per-head factor of the scores (scale * log2(e) / rms(q)), published with q~
+    {
+      const volatile int* qgen = reinterpret_cast<const volatile int*>(c.sm + SM_QGEN);
+      bool ok = true;
+      if (qgen[b] != (int)seq + 1) {
+        const unsigned long long start = clock64();
+        while (qgen[b] != (int)seq + 1) {
+          __nanosleep(200);
+          if (c.misc[M_ABORT]) { ok = false; break; }
+          if (clock64() - start > WAIT_LIMIT_CYCLES) {
+            atomicOr(c.status, DSA_STATUS_WAIT_TIMEOUT);
+            c.misc[M_ABORT] = 1;
+            ok = false;
+            break;
+          }
+        }
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      __threadfence_block();
+    }
+    const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
     if (r < 64) s_m[r] = -INFINITY;
     if (!grp.sync(c)) return;
 #pragma unroll 1
@@ -530,25 +679,48 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       const bool valid = r < nrows - tt * TILE;
       if (!wait_bar_w(c, B_SFULL + sb, (g >> 1) & 1)) return;
       tc_fence_after();
-      bool need = tt == 0;
-      if (!need) {
-        // pass 1: how far does this tile exceed the reference max of each head?
+      // the P buffer is free once PV of the previous tile has completed (in practice it
+      // has: the tensor core ran that PV before this tile's QK^T)
+      if (!wait_bar_w(c, B_PFREE, (g & 1) ^ 1)) return;
+      const uint32_t prow = c.sb + SM_P + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+      const uint32_t rsw = (uint32_t)(r & 7);
+      // P = exp2(S - m) in fp16 into row r of the MN-major B operand; returns the largest
+      // S - m of the row, i.e. how far the tile exceeds the reference max
+      auto p_pass = [&]() -> float {
         float dmax = -INFINITY;
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t a[32];
-          tmem_ld32(ts + 32 * hf, a);
-          const float4* m4 = reinterpret_cast<const float4*>(s_m + 32 * hf);
-          float m[32];
+        for (int hq = 0; hq < 4; ++hq) {   // 16 heads at a time
+          uint32_t a[16];
+          tmem_ld16(ts + 16 * hq, a);
+          const float4* m4 = reinterpret_cast<const float4*>(s_m + 16 * hq);
+          const float4* f4 = reinterpret_cast<const float4*>(s_inv + 16 * hq);
+          float m[16], fi[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = m4[q];
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = m4[q], g2 = f4[q];
             m[4 * q] = f.x; m[4 * q + 1] = f.y; m[4 * q + 2] = f.z; m[4 * q + 3] = f.w;
+            fi[4 * q] = g2.x; fi[4 * q + 1] = g2.y; fi[4 * q + 2] = g2.z; fi[4 * q + 3] = g2.w;
           }
           tc_wait_ld();
+          uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) dmax = fmaxf(dmax, (valid ? __uint_as_float(a[i]) : -INFINITY) - m[i]);
+          for (int i = 0; i < 8; ++i) {
+            const float x0 = valid ? fmaf(__uint_as_float(a[2 * i]), fi[2 * i], -m[2 * i]) : -INFINITY;
+            const float x1 = valid ? fmaf(__uint_as_float(a[2 * i + 1]), fi[2 * i + 1], -m[2 * i + 1]) : -INFINITY;
+            dmax = fmaxf(dmax, fmaxf(x0, x1));
+            pk[i] = pack_f16x2(exp2f(x0), exp2f(x1));
+          }
+          const uint32_t c0 = (uint32_t)(2 * hq);
+          sts128(prow + ((c0 ^ rsw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          sts128(prow + (((c0 + 1) ^ rsw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
         }
+        return dmax;
+      };
+      bool need = tt == 0;
+      if (!need) {
+        // optimistic pass with the current reference max; redone below if the tile
+        // exceeds it by more than 2^8 somewhere
+        float dmax = p_pass();
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xFFFFFFFFu, dmax, o));
         if (lane == 0) s_flag[4 * (g & 1) + q4] = dmax;
@@ -557,17 +729,24 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         need = !(fmaxf(fmaxf(fl[0], fl[1]), fmaxf(fl[2], fl[3])) <= 8.0f);
       }
       if (need) {
-        // exact tile max per head, new reference max, rescale factors
+        // exact tile max per head, new reference max, rescale factors, P again
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t a[32];
-          tmem_ld32(ts + 32 * hf, a);
+        for (int hq = 0; hq < 4; ++hq) {
+          uint32_t a[16];
+          tmem_ld16(ts + 16 * hq, a);
+          const float4* f4 = reinterpret_cast<const float4*>(s_inv + 16 * hq);
           tc_wait_ld();
-          float v[32];
+          float v[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(a[i]) : -INFINITY;
-          reduce32<true>(v, lane);
-          s_red[q4 * 64 + 32 * hf + lane] = v[0];
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = f4[q];
+            v[4 * q] = valid ? __uint_as_float(a[4 * q]) * f.x : -INFINITY;
+            v[4 * q + 1] = valid ? __uint_as_float(a[4 * q + 1]) * f.y : -INFINITY;
+            v[4 * q + 2] = valid ? __uint_as_float(a[4 * q + 2]) * f.z : -INFINITY;
+            v[4 * q + 3] = valid ? __uint_as_float(a[4 * q + 3]) * f.w : -INFINITY;
+          }
+          reduce16<true>(v, lane);          // lanes 2m, 2m + 1: head 16 hq + m
+          if ((lane & 1) == 0) s_red[q4 * 64 + 16 * hq + (lane >> 1)] = v[0];
         }
         if (!grp.sync(c)) return;
         if (r < 64) {
@@ -578,36 +757,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
           s_alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
         }
         if (!grp.sync(c)) return;
-      }
-      // the P buffer is free once PV of the previous tile has completed
-      if (!wait_bar_w(c, B_PFREE, (g & 1) ^ 1)) return;
-      // pass 2: P = exp2(S - m) in fp16, row r of the MN-major B operand
-      const uint32_t prow = c.sb + SM_P + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t a[32];
-        tmem_ld32(ts + 32 * hf, a);
-        const float4* m4 = reinterpret_cast<const float4*>(s_m + 32 * hf);
-        float m[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 f = m4[q];
-          m[4 * q] = f.x; m[4 * q + 1] = f.y; m[4 * q + 2] = f.z; m[4 * q + 3] = f.w;
-        }
-        tc_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = valid ? __uint_as_float(a[2 * i]) : -INFINITY;
-          const float x1 = valid ? __uint_as_float(a[2 * i + 1]) : -INFINITY;
-          pk[i] = pack_f16x2(exp2f(x0 - m[2 * i]), exp2f(x1 - m[2 * i + 1]));
-        }
-        const uint32_t rsw = (uint32_t)(r & 7);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint32_t chunk = (uint32_t)(4 * hf + cc);
-          sts128(prow + ((chunk ^ rsw) << 4), make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]));
-        }
+        p_pass();
       }
       tc_fence_before();
       mbar_arrive(bar(c, B_SFREE + sb));     // S^T fully read
@@ -633,7 +783,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         }
         tc_wait_st();
       }
-      if (tt == T - 1 && r < 64) reinterpret_cast<float*>(c.sm + SM_MFIN)[64 * b + r] = s_m[r];
+      if (tt == T - 1 && r < 64) reinterpret_cast<float*>(c.sm + SM_MFIN)[64 * (nq & 1) + r] = s_m[r];
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(c, B_PFULL));
@@ -646,184 +796,108 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
     ++seq;
+    ++nq;
     if (open_item() <= 0) return;
   }
 }
 
 // ================================================================== EPI
-// 1/rms of every head of q[t] (fp32 statistics) times softmax_scale * log2(e): eight
-// lanes per head, sixteen heads per pass of the 128 threads.
-DSA_DEV void q_stats(const KParams& P, const Ctx& c, int b, int er, Group& grp) {
-  const int t = item_info(c, b)[IT_TOKEN];
-  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
-  const int hs = er >> 3, sl = er & 7;
-#pragma unroll 1
-  for (int it = 0; it < 4; ++it) {
-    uint4 raw[1][9];
-#pragma unroll
-    for (int u = 0; u < 1; ++u) {
-      const int h = 16 * (it + u) + hs;
-#pragma unroll
-      for (int k = 0; k < 9; ++k)
-        raw[u][k] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + (sl + 8 * k) * 8)
-                                : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < 1; ++u) {
-      const int h = 16 * (it + u) + hs;
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < 9; ++k) {
-        const uint32_t w4[4] = {raw[u][k].x, raw[u][k].y, raw[u][k].z, raw[u][k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = __uint_as_float(w4[e] << 16), bb = __uint_as_float(w4[e] & 0xFFFF0000u);
-          ss = fmaf(a, a, fmaf(bb, bb, ss));
-        }
-      }
-      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
-      if (sl == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(ss * (1.0f / D_QK) + P.rms_eps) * P.score_scale_log2 : 0.f;
-    }
-  }
-  grp.sync(c);
-}
+// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
+// operand of QK^T.  The per-head factor softmax_scale * log2(e) / rms(q) multiplies the
+// scores instead (the rotation and QK^T are linear in q~), so the statistics need not come
+// first.  64 heads x 9 atoms x 8 chunks of 8 dims: thread-piece j covers head
+// (er / 8) + 16 (j % 4), chunk er % 8, atom j / 4, so one warp reads four 128-byte head
+// rows and writes them with conflict-free swizzled stores.  Chunk c of the latent dims
+// (atoms 2c, 2c + 1) is announced on QRDY[c], the rotary atom on QRDY[4], so that QK^T
+// can start before the whole of q~ is written; the statistics follow.
+struct QArgs {
+  const uint16_t* q;
+  const uint16_t* norm_w;
+  int h_q;
+  float eps, c2;
+};
 
-// q~ of one item: 64 heads x 9 atoms x 8 chunks of 8 dims; thread-piece p covers head
-// (p / 8) % 64, chunk p % 8, atom p / 512, so one warp reads four 128-byte head rows and
-// writes them with conflict-free swizzled stores.
-DSA_DEV void build_q(const KParams& P, const Ctx& c, int b, int er) {
+DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, uint32_t seq, int er, Group& grp) {
   const int* info = item_info(c, b);
   const int t = info[IT_TOKEN];
-  const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
   const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-  const uint16_t* s_w = reinterpret_cast<const uint16_t*>(c.sm + SM_NORMW);
+  const int hs = er >> 3, chn = er & 7;
+  const uint16_t* qt = P.q + (size_t)t * P.h_q * D_QK;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};
+  // rounds of two atoms: eight q pieces (four heads x two atoms) and two norm-weight
+  // pieces in flight per thread
 #pragma unroll 1
-  for (int j0 = 0; j0 < 36; j0 += 9) {
-    uint4 raw[9];
+  for (int a0 = 0; a0 < 9; a0 += 2) {
+    const int na = a0 < 8 ? 2 : 1;
+    uint4 raw[2][4], wq[2];
 #pragma unroll
-    for (int u = 0; u < 9; ++u) {
-      const int p = er + 128 * (j0 + u);
-      const int a = p >> 9, h = (p >> 3) & 63, chn = p & 7;
-      raw[u] = (h < P.h_q) ? ldg_nc(P.q + ((size_t)t * P.h_q + h) * D_QK + 64 * a + 8 * chn)
-                           : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 2; ++j) {
+      if (j >= na) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int h = hs + 16 * k;
+        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
+      }
+      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
     }
 #pragma unroll
-    for (int u = 0; u < 9; ++u) {
-      const int p = er + 128 * (j0 + u);
-      const int a = p >> 9, h = (p >> 3) & 63, chn = p & 7;
-      const int d0 = 64 * a + 8 * chn;
-      const float inv = s_inv[h];
-      const uint4 wv = *reinterpret_cast<const uint4*>(s_w + d0);
-      const uint32_t x4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-      const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-      float x[8];
+    for (int j = 0; j < 2; ++j) {
+      if (j >= na) break;
+      const int a = a0 + j;
+      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = __uint_as_float(x4[e] << 16) * inv * __uint_as_float(w4[e] << 16);
-        x[2 * e + 1] = __uint_as_float(x4[e] & 0xFFFF0000u) * inv * __uint_as_float(w4[e] & 0xFFFF0000u);
-      }
-      if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+      for (int k = 0; k < 4; ++k) {
+        const uint4 cu = raw[j][k];
+        const int h = hs + 16 * k;
+        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
+        float x[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 cs = rope[4 * chn + e];
-          const float x0 = x[2 * e], x1 = x[2 * e + 1];
-          x[2 * e] = x0 * cs.x - x1 * cs.y;
-          x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
+          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
+          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
+          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
         }
+        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 cs = rope[4 * chn + e];
+            const float x0 = x[2 * e], x1 = x[2 * e + 1];
+            x[2 * e] = x0 * cs.x - x1 * cs.y;
+            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+          }
+        }
+        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                   pack_f16x2(x[6], x[7]));
+        sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
       }
-      const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                 pack_f16x2(x[6], x[7]));
-      sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
+      if ((a & 1) == 1 || a == 8) {
+        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
+        fence_async_smem();
+        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
+      }
     }
   }
-  fence_async_smem();
+  // per-head statistics: eight lanes hold the pieces of head hs + 16 k
+  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v = ss[k];
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    const int h = hs + 16 * k;
+    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
+  }
+  grp.sync(c);
+  if (er == 0) {
+    __threadfence_block();
+    reinterpret_cast<volatile int*>(c.sm + SM_QGEN)[b] = (int)seq + 1;
+  }
 }
 
-// Finish 32 consecutive output dims of one head in one thread: inverse RoPE, optional
-// pre-cast store, MXFP8 (one 32-value block) and the stores.
-DSA_DEV void finalize_block(const KParams& P, float (&v)[32], int t, int h, int d0, const float2* rope) {
-  if (d0 >= 448) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float2 cs = rope[((d0 - 448) >> 1) + k];
-      const float x0 = v[2 * k], x1 = v[2 * k + 1];
-      v[2 * k] = fmaf(x1, cs.y, x0 * cs.x) + 0.0f;     // +0.0f: a rotated exact zero stays +0
-      v[2 * k + 1] = fmaf(-x0, cs.y, x1 * cs.x) + 0.0f;
-    }
-  }
-  const size_t row = (size_t)t * P.h_q + h;
-  if (P.out_precast) {
-    float4* dst = reinterpret_cast<float4*>(P.out_precast + row * D_LAT + d0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
-  int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 8;   // floor(log2 amax) - 8
-  E = E < -127 ? -127 : E;
-  const float inv = __uint_as_float((uint32_t)(127 - E) << 23);    // 2^-E, exact
-  uint32_t wq[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t lo = f32x2_to_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv);
-    const uint32_t hi = f32x2_to_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv);
-    wq[k] = lo | (hi << 16);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(P.out_fp8 + row * D_LAT + d0);
-  dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-  dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-  P.out_sf[row * 16 + (d0 >> 5)] = (uint8_t)(E + 127);
-}
-
-// Finish dim d of heads h0..h0+31 held one head per register (the warp holds one
-// 32-dim MXFP8 block of each head): inverse RoPE with the neighbouring lane, optional
-// pre-cast store, block amax across the warp, scale codes and E4M3 codes.  Stores of
-// one head from the 32 lanes are contiguous.
-DSA_DEV void finalize_lanes(const KParams& P, const Ctx& c, float (&v)[32], int t, int h0, int d, int e, int lane,
-                            const float2* rope) {
-  if (d >= 448) {
-    const float2 cs = rope[(d - 448) >> 1];
-    const bool odd = d & 1;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
-      // pair (x0, x1) rotated by -angle: (x0 c + x1 s, -x0 s + x1 c)
-      v[i] = odd ? fmaf(-o, cs.y, v[i] * cs.x) + 0.0f : fmaf(o, cs.y, v[i] * cs.x) + 0.0f;
-    }
-  }
-  const size_t row0 = (size_t)t * P.h_q;
-  if (P.out_precast) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (h0 + i < P.h_q) P.out_precast[(row0 + h0 + i) * D_LAT + d] = v[i];
-  }
-  float am[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) am[i] = fabsf(v[i]);
-  reduce32<true>(am, lane);           // lane L: amax of head h0 + L
-  int E = (int)((__float_as_uint(am[0]) >> 23) & 0xFF) - 127 - 8;
-  E = E < -127 ? -127 : E;
-  float* s_scl = reinterpret_cast<float*>(c.sm + SM_ESCL) + 32 * e;
-  s_scl[lane] = __uint_as_float((uint32_t)(127 - E) << 23);
-  if (h0 + lane < P.h_q) P.out_sf[(row0 + h0 + lane) * 16 + (d >> 5)] = (uint8_t)(E + 127);
-  __syncwarp();
-  const float4* s4 = reinterpret_cast<const float4*>(s_scl);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 f = s4[q];
-    const uint32_t lo = f32x2_to_e4m3x2(v[4 * q] * f.x, v[4 * q + 1] * f.y);
-    const uint32_t hi = f32x2_to_e4m3x2(v[4 * q + 2] * f.z, v[4 * q + 3] * f.w);
-    const uint8_t b4[4] = {(uint8_t)lo, (uint8_t)(lo >> 8), (uint8_t)hi, (uint8_t)(hi >> 8)};
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (h0 + 4 * q + k < P.h_q) P.out_fp8[(row0 + h0 + 4 * q + k) * D_LAT + d] = b4[k];
-  }
-  __syncwarp();
-}
-
+// The epilogue reads O^T out of TMEM one dim per lane, 16 heads at a time, and finishes
+// it from registers; each 64-head column block of TMEM is released as soon as it is read.
 DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int lane) {
   const int er = e * 32 + lane;
   const uint32_t tlane = (uint32_t)(e * 32) << 16;
@@ -832,32 +906,30 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
   const float ln2 = 0.69314718055994531f;
   const bool is_split = P.n_splits > 1;
   Group grp{B_EPG, 0};
-  uint32_t nq = 0;
+  const QArgs qa{P.q, P.norm_w, P.h_q, P.rms_eps, P.score_scale_log2};
+  uint32_t nq = 0;   // items with tiles
   int built = -1;
   for (uint32_t seq = 0;; ++seq) {
-    const int b = seq & 1;
-    if (!wait_bar_w(c, B_ITFULL + b, (seq >> 1) & 1)) return;
+    const int b = seq % NB;
+    if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return;
     const int* info = item_info(c, b);
     if (info[IT_ITEM] < 0) return;
     const int t = info[IT_TOKEN], split = info[IT_SPLIT], T = info[IT_T];
-    const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
     if (T > 0) {
       if (built != (int)seq) {
-        q_stats(P, c, b, er, grp);
         if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return;
-        build_q(P, c, b, er);
-        mbar_arrive(bar(c, B_QREADY));
+        build_q(qa, c, b, seq, er, grp);
       }
-      // build the next item's q~ as soon as this item's QK^T no longer reads it
+      // the next item's q~ as soon as this item's QK^T no longer reads the buffer
       {
-        const int nb = b ^ 1;
-        if (!wait_bar_w(c, B_ITFULL + nb, ((seq + 1) >> 1) & 1)) return;
+        const int nb = (seq + 1) % NB;
+        if (!wait_bar_w(c, B_ITFULL + nb, ((seq + 1) / NB) & 1)) return;
         const int* ninfo = item_info(c, nb);
         if (ninfo[IT_ITEM] >= 0 && ninfo[IT_T] > 0) {
-          q_stats(P, c, nb, er, grp);
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + (size_t)ninfo[IT_TOKEN] * P.h_q * D_QK);
+          for (int l = er; l < P.h_q * 9; l += N_EPI) prefetch_line_l2(qn + 128 * l);
           if (!wait_bar_w(c, B_QFREE, nq & 1)) return;
-          build_q(P, c, nb, er);
-          mbar_arrive(bar(c, B_QREADY));
+          build_q(qa, c, nb, seq + 1, er, grp);
           built = (int)seq + 1;
         }
       }
@@ -880,7 +952,7 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       if (!grp.sync(c)) return;
       if (er < 64) {
         const float l = s_el[er];
-        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[64 * b + er];
+        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[64 * (nq & 1) + er];
         const bool any = l > 0.f;
         s_else[er] = any ? mfin + log2f(l) : -INFINITY;
         s_el[er] = any ? 1.f / l : 0.f;
@@ -888,22 +960,25 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       if (!grp.sync(c)) return;
       if (!is_split && P.out_lse && er < P.h_q) P.out_lse[(size_t)t * P.h_q + er] = s_else[er] * ln2;
       if (is_split && er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = s_else[er];
+      const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
+      const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+      float* part = is_split ? P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT : nullptr;
 #pragma unroll 1
       for (int cidx = 0; cidx < 4; ++cidx) {
         const int d = 128 * cidx + 32 * e + lane;
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t a[32];
-          tmem_ld32(tmem + tlane + TM_O + 64 * cidx + 32 * hf, a);
+        for (int hq = 0; hq < 4; ++hq) {
+          uint32_t a[16];
+          tmem_ld16(tmem + tlane + TM_O + 64 * cidx + 16 * hq, a);
           tc_wait_ld();
-          if (hf == 1) {
+          if (hq == 3) {
             tc_fence_before();
             mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
           }
-          float v[32];
-          const float4* il4 = reinterpret_cast<const float4*>(s_el + 32 * hf);
+          const float4* il4 = reinterpret_cast<const float4*>(s_el + 16 * hq);
+          float v[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 4; ++q) {
             const float4 f = il4[q];
             v[4 * q] = __uint_as_float(a[4 * q]) * f.x;
             v[4 * q + 1] = __uint_as_float(a[4 * q + 1]) * f.y;
@@ -911,11 +986,11 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
             v[4 * q + 3] = __uint_as_float(a[4 * q + 3]) * f.w;
           }
           if (is_split) {
-            float* dst = P.part_o + (((size_t)t * P.n_splits + split) * HP + 32 * hf) * D_LAT + d;
+            float* o = part + (size_t)(16 * hq) * D_LAT + d;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[(size_t)i * D_LAT] = v[i];
+            for (int i = 0; i < 16; ++i) o[(size_t)i * D_LAT] = v[i];
           } else {
-            finalize_lanes(P, c, v, t, 32 * hf, d, e, lane, rope);
+            finalize_lanes(O, v, t, 16 * hq, d, lane, rope);
           }
         }
       }
@@ -1014,7 +1089,7 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int tid) {
         v[4 * k + 3] = fmaf(w0, f0[k].w, fmaf(w1, f1[k].w, v[4 * k + 3]));
       }
     }
-    finalize_block(P, v, t, h, 32 * blk, rope);
+    finalize_block(OutPtrs{P.out_fp8, P.out_sf, P.out_precast, P.h_q}, v, t, h, 32 * blk, rope);
   }
 }
 
@@ -1042,13 +1117,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
       mbar_init(bar(c, B_KRFREE + i), 1);
       mbar_init(bar(c, B_SFULL + i), 1);
       mbar_init(bar(c, B_SFREE + i), N_SM);
+    }
+    for (int i = 0; i < NB; ++i) {
       mbar_init(bar(c, B_ITFULL + i), N_PREP);
       mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SM + N_EPI + 1);
     }
     mbar_init(bar(c, B_PFULL), N_SM);
     mbar_init(bar(c, B_PFREE), 1);
     mbar_init(bar(c, B_ODONE), 1);
-    mbar_init(bar(c, B_QREADY), N_EPI);
+    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_EPI);
     mbar_init(bar(c, B_QFREE), 1);
     mbar_init(bar(c, B_MFIN), N_SM);
     mbar_init(bar(c, B_SMG), N_SM);
@@ -1057,11 +1134,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
     c.misc[M_LAST] = 0;
+    for (int i = 0; i < NB; ++i) reinterpret_cast<volatile int*>(c.sm + SM_QGEN)[i] = 0;
   }
   if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
   {
-    uint16_t* s_w = reinterpret_cast<uint16_t*>(c.sm + SM_NORMW);
-    for (int i = tid; i < D_QK; i += NTHREADS) s_w[i] = P.norm_w[i];
     uint32_t* ones = reinterpret_cast<uint32_t*>(c.sm + SM_ONES);
     for (int i = tid; i < 1024; i += NTHREADS) ones[i] = 0x3C003C00u;   // fp16 1.0 pairs
     fence_async_smem();
@@ -1079,7 +1155,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     epi_role(P, c, tmem, warp - W_EPI, lane);
   } else if (warp == W_MMA) {
     if (lane == 0) mma_role(P, c, tmem);
-  } else {
+  } else if (warp == W_PREP) {
     prep_role(P, c, lane);
   }
 
@@ -1089,7 +1165,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     // every MMA this CTA issued has completed before TMEM is released
     tc_commit(bar(c, B_DRAIN));
     const unsigned long long start = clock64();
-    while (!mbar_try(bar(c, B_DRAIN), 0) && clock64() - start < WAIT_LIMIT_CYCLES) {
+    while (!mbar_wait_susp(bar(c, B_DRAIN), 0) && clock64() - start < WAIT_LIMIT_CYCLES) {
     }
   }
   tc_fence_before();
@@ -1127,7 +1203,7 @@ static Layout layout_for(int s_q, int n_splits, int num_sms) {
   L.counters_off = 256;
   size_t off = up(L.counters_off + 4 * (size_t)(s_q > 0 ? s_q : 1));
   L.lists_off = off;
-  off = up(off + (size_t)num_sms * 2 * DSA_MAX_TOPK * 4);
+  off = up(off + (size_t)num_sms * NB * DSA_MAX_TOPK * 4);
   if (n_splits > 1) {
     L.part_o_off = off;
     off = up(off + (size_t)s_q * n_splits * HP * D_LAT * 4);
