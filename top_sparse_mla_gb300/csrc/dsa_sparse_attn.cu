@@ -384,33 +384,32 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[16], int t, int h0, int
 // dims); the four rows of one store instruction alternate in row parity, which keeps the
 // stores free of bank conflicts.  Raw bytes are loaded two chunks ahead of their
 // conversion (chunk c of a tile lives in register slot c % 2).
+// An entry for a row past the end of the item: no list entry has every bit set, since
+// pools hold fewer than 2^31 rows.
+constexpr uint32_t NO_ROW = 0xFFFFFFFFu;
 struct DqRows {
-  uint32_t e[4];   // list entries of rows 16 w + 4 k + sub
-  bool v[4];
-  uint32_t es;     // lanes ch < 4: entry of row 16 w + 4 ch + sub (its scales)
-  bool vs;
+  uint32_t e[4];   // list entries of rows 16 w + 4 k + sub, or NO_ROW
+  uint32_t es;     // lanes ch < 4: entry of row 16 w + 4 ch + sub (its scales), or NO_ROW
 };
 
 DSA_DEV void dq_load_rows(const uint32_t* list, int tt, int nrows, int w, int sub, int ch, DqRows& R) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int r = tt * TILE + 16 * w + 4 * k + sub;
-    R.v[k] = r < nrows;
-    R.e[k] = R.v[k] ? __ldcg(list + r) : 0u;
+    R.e[k] = r < nrows ? __ldcg(list + r) : NO_ROW;
   }
   const int rs = tt * TILE + 16 * w + 4 * (ch & 3) + sub;
-  R.vs = ch < 4 && rs < nrows;
-  R.es = R.vs ? __ldcg(list + rs) : 0u;
+  R.es = (ch < 4 && rs < nrows) ? __ldcg(list + rs) : NO_ROW;
 }
 
 DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const DqRows& R, int ch) {
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    dst[k] = R.v[k] ? ldg_nc(row_ptr(P, R.e[k]) + 128 * cidx + 16 * ch) : make_uint4(0, 0, 0, 0);
+    dst[k] = R.e[k] != NO_ROW ? ldg_nc(row_ptr(P, R.e[k]) + 128 * cidx + 16 * ch) : make_uint4(0, 0, 0, 0);
 }
 
 DSA_DEV uint4 dq_load_scales(const KParams& P, const DqRows& R) {
-  return R.vs ? ldg_nc(row_ptr(P, R.es) + D_LAT) : make_uint4(0, 0, 0, 0);
+  return R.es != NO_ROW ? ldg_nc(row_ptr(P, R.es) + D_LAT) : make_uint4(0, 0, 0, 0);
 }
 
 DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
@@ -486,7 +485,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
           // the six 128-byte lines of each next row, one line per lane
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            if (nxt.v[k]) prefetch_line_l2(row_ptr(P, nxt.e[k]) + 128 * ch);
+            if (nxt.e[k] != NO_ROW) prefetch_line_l2(row_ptr(P, nxt.e[k]) + 128 * ch);
         }
         // the chunk two ahead
         if (cidx < 2) {
