@@ -10,15 +10,15 @@
 //                      memory, fp32 block scale folded in.  The one tile is the A operand
 //                      of both contractions: K-major for QK^T (M = rows), MN-major for PV
 //                      (M = dims).  Raw bytes are loaded two chunks ahead, rows are
-//                      prefetched into L2 one tile ahead.  Between items: the MXFP8 finish
-//                      of the previous item's output block (inverse RoPE, scales, E4M3).
-//   SM   (warps 8-11)  softmax over S^T (lazy running max, exp2, fp16 P) with the per-head
-//                      factor softmax_scale * log2(e) / rms(q); the rotary part of the next
-//                      tile's keys (bf16 -> fp16) into TMEM
-//   EPI  (warps 12-15) q~ = RoPE(q * w) in fp16 as the B operand of QK^T, chunk by chunk,
-//                      built for the next item while the current one finishes, and the
-//                      fp32 RMS statistics of q; the epilogue: O^T / l out of TMEM into a
-//                      global output block (or the split partial)
+//                      prefetched into L2 one tile ahead.  Between items (no splits): the
+//                      MXFP8 finish of output dims 128..383 of the previous item.
+//   SM   (warps 8-11)  when an item opens: q~ = RoPE(q * w) in fp16 as the B operand of
+//                      QK^T, chunk by chunk, and the fp32 RMS statistics of q; then per
+//                      tile the softmax over S^T (lazy running max, exp2, fp16 P) with the
+//                      per-head factor softmax_scale * log2(e) / rms(q), and the rotary
+//                      part of the next tile's keys (bf16 -> fp16) into TMEM
+//   EPI  (warps 12-15) 1/l and the LSE; the epilogue: O^T / l out of TMEM into the global
+//                      output (dims 0..127 and 384..511, or all of it as a split partial)
 //   MMA  (warp 16)     S^T[128 rows x 64 heads] = K~ . q~^T; O^T[512 x 64] += V~^T . P;
 //                      l[64] += 1^T . P (row sums on the tensor core)
 //   PREP (warp 17)     take an item, compact its valid index columns into a row list,
@@ -74,8 +74,7 @@ constexpr uint32_t SM_ESCL = SM_RED + 1024;        // 4 EPI warps x 32 fp32 bloc
 constexpr uint32_t SM_EL = SM_ESCL + 512;          // 64 fp32 row sums, then 1/l
 constexpr uint32_t SM_ELSE = SM_EL + 256;          // 64 fp32 LSE (log2 units)
 constexpr uint32_t SM_FLAG = SM_ELSE + 256;        // 2 x 4 fp32
-constexpr uint32_t SM_QGEN = SM_FLAG + 32;         // NB ints: q statistics of item seq ready (seq + 1)
-constexpr uint32_t SM_MISC = SM_QGEN + 16;         // misc ints
+constexpr uint32_t SM_MISC = SM_FLAG + 32;         // misc ints
 constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
 constexpr uint32_t SM_END = SM_BAR + 48 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
@@ -87,7 +86,7 @@ enum {
   B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
   B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
   B_ITFULL, B_ITEMPTY = B_ITFULL + NB, B_ODONE = B_ITEMPTY + NB, B_OFREE,
-  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_MFIN, B_SMG, B_EPG, B_DRAIN, B_COUNT
+  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_MFIN, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_COUNT
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
@@ -335,16 +334,17 @@ DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int 
   O.sf[row * 16 + (d0 >> 5)] = (uint8_t)(E + 127);
 }
 
-// Finish dim d of heads h0..h0+15, one head per register; the 32 lanes of the warp hold
+// Finish dim d of heads h0..h0+N-1, one head per register; the 32 lanes of the warp hold
 // one 32-dim MXFP8 block of each head.  Inverse RoPE with the neighbouring lane, optional
 // pre-cast store, block amax across the warp (redux), UE8M0 code, E4M3 codes.  A head's
 // stores from the 32 lanes are contiguous.
-DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[16], int t, int h0, int d, int lane, const float2* rope) {
+template <int N>
+DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[N], int t, int h0, int d, int lane, const float2* rope) {
   if (d >= 448) {
     const float2 cs = rope[(d - 448) >> 1];
     const bool odd = d & 1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < N; ++i) {
       const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
       // pair (x0, x1) rotated by -angle: (x0 c + x1 s, -x0 s + x1 c)
       v[i] = odd ? fmaf(-o, cs.y, v[i] * cs.x) + 0.0f : fmaf(o, cs.y, v[i] * cs.x) + 0.0f;
@@ -354,13 +354,13 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[16], int t, int h0, int
   if (O.precast) {
     float* pc = O.precast + row0 * D_LAT + d;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < N; ++i)
       if (h0 + i < O.h_q) pc[(size_t)i * D_LAT] = v[i];
   }
   uint8_t* out = O.fp8 + row0 * D_LAT + d;
-  uint32_t sfw = 0;   // this lane's scale code (lane i < 16: head h0 + i)
+  uint32_t sfw = 0;   // this lane's scale code (lane i < N: head h0 + i)
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
+  for (int i = 0; i < N; i += 2) {
     float am0, am1;
     asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(am0) : "f"(v[i]));
     asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(am1) : "f"(v[i + 1]));
@@ -374,7 +374,49 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[16], int t, int h0, int
     if (h0 + i + 1 < O.h_q) out[(size_t)(i + 1) * D_LAT] = (uint8_t)(q >> 8);
     sfw = lane == i ? (uint32_t)(e0 + 127) : (lane == i + 1 ? (uint32_t)(e1 + 127) : sfw);
   }
-  if (lane < 16 && h0 + lane < O.h_q) O.sf[(row0 + lane) * 16 + (d >> 5)] = (uint8_t)sfw;
+  if (lane < N && h0 + lane < O.h_q) O.sf[(row0 + lane) * 16 + (d >> 5)] = (uint8_t)sfw;
+}
+
+// Epilogue of the 128-dim column block cidx of O^T by a warp on TMEM lane quarter q4
+// (dims 128 cidx + 32 q4 + lane), NH heads at a time, scaled by 1/l from s_il.  The
+// block is released on OFREE[cidx] once it and s_il have been read.  With part set the
+// normalised partial is stored instead of finished.
+template <int NH>
+DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, const float* s_il, const OutPtrs& O,
+                       int t, float* part, const float2* rope) {
+  const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
+  const int d = 128 * cidx + 32 * q4 + lane;
+#pragma unroll 1
+  for (int hg = 0; hg < 64 / NH; ++hg) {
+    uint32_t a[NH];
+    if constexpr (NH == 16) {
+      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
+    } else {
+      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
+    }
+    tc_wait_ld();
+    const float4* il4 = reinterpret_cast<const float4*>(s_il + NH * hg);
+    float v[NH];
+#pragma unroll
+    for (int q = 0; q < NH / 4; ++q) {
+      const float4 f = il4[q];
+      v[4 * q] = __uint_as_float(a[4 * q]) * f.x;
+      v[4 * q + 1] = __uint_as_float(a[4 * q + 1]) * f.y;
+      v[4 * q + 2] = __uint_as_float(a[4 * q + 2]) * f.z;
+      v[4 * q + 3] = __uint_as_float(a[4 * q + 3]) * f.w;
+    }
+    if (hg == 64 / NH - 1) {
+      tc_fence_before();
+      mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
+    }
+    if (part) {
+      float* o = part + (size_t)(NH * hg) * D_LAT + d;
+#pragma unroll
+      for (int i = 0; i < NH; ++i) o[(size_t)i * D_LAT] = v[i];
+    } else {
+      finalize_lanes<NH>(O, v, t, NH * hg, d, lane, rope);
+    }
+  }
 }
 
 // ================================================================== DQ
@@ -412,7 +454,7 @@ DSA_DEV uint4 dq_load_scales(const KParams& P, const DqRows& R) {
   return R.es != NO_ROW ? ldg_nc(row_ptr(P, R.es) + D_LAT) : make_uint4(0, 0, 0, 0);
 }
 
-DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
+DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int lane) {
   const int sub = lane >> 3, ch = lane & 7;
   const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
   const uint32_t c0 = (uint32_t)(2 * (ch & 3));
@@ -420,6 +462,27 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
   uint4 scl;
   DqRows cur, nxt;
   uint32_t g = 0, seq = 0;
+  // Without splits the dequant warps finish column blocks 1 (warps 0-3) and 2 (warps
+  // 4-7) of each item's O^T, right after converting the next item's first tile: that
+  // item's PV waits for O^T to be read, and the warps would wait for that PV anyway.
+  // The item's buffers are released after its share.
+  const bool share = P.n_splits == 1;
+  int pend = -1;          // item (sequence number) whose share is still to do
+  uint32_t pend_nq = 0;   // its index among the items with tiles
+  uint32_t nq = 0;
+  auto do_share = [&]() -> bool {
+    const int pb = pend % NB;
+    if (!wait_bar_w(c, B_ODONE, pend_nq & 1)) return false;
+    if (!wait_bar_w(c, B_LREADY, pend_nq & 1)) return false;
+    tc_fence_after();
+    const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
+    const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * pb;
+    epi_chunk<8>(c, tmem, w & 3, lane, 1 + (w >> 2), reinterpret_cast<const float*>(c.sm + SM_EL), O,
+                 item_info(c, pb)[IT_TOKEN], nullptr, rope);
+    mbar_arrive(bar(c, B_ITEMPTY + pb));
+    pend = -1;
+    return true;
+  };
   // next item with tiles: its info waited for, rows of tile 0 and its first two chunks
   // in flight
   auto open_item = [&]() -> int {   // 1 = opened, 0 = no more items, -1 = aborted
@@ -499,11 +562,19 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, int w, int lane) {
         cur = nxt;
       }
       ++g;
+      if (tt == 0 && pend >= 0 && !do_share()) return;
     }
-    mbar_arrive(bar(c, B_ITEMPTY + b));
+    if (share) {
+      pend = (int)seq;
+      pend_nq = nq;
+    } else {
+      mbar_arrive(bar(c, B_ITEMPTY + b));
+    }
+    ++nq;
     ++seq;
     r = open_item();
   }
+  if (r == 0 && pend >= 0) do_share();
 }
 
 // ================================================================== MMA issuer
@@ -591,6 +662,95 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   }
 }
 
+// ================================================================== q~
+// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
+// operand of QK^T.  The per-head factor softmax_scale * log2(e) / rms(q) multiplies the
+// scores instead (the rotation and QK^T are linear in q~), so the statistics need not come
+// first.  64 heads x 9 atoms x 8 chunks of 8 dims: thread-piece j covers head
+// (er / 8) + 16 (j % 4), chunk er % 8, atom j / 4, so one warp reads four 128-byte head
+// rows and writes them with conflict-free swizzled stores.  Chunk c of the latent dims
+// (atoms 2c, 2c + 1) is announced on QRDY[c], the rotary atom on QRDY[4], so that QK^T
+// can start before the whole of q~ is written; the statistics follow.
+struct QArgs {
+  const uint16_t* q;
+  const uint16_t* norm_w;
+  int h_q;
+  float eps, c2;
+};
+
+DSA_DEV bool build_q(const QArgs& P, const Ctx& c, int b, int er, Group& grp) {
+  const uint16_t* qt = P.q + (size_t)item_info(c, b)[IT_TOKEN] * P.h_q * D_QK;
+  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  const int hs = er >> 3, chn = er & 7;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};
+  // rounds of two atoms: eight q pieces (four heads x two atoms) and two norm-weight
+  // pieces in flight per thread
+#pragma unroll 1
+  for (int a0 = 0; a0 < 9; a0 += 2) {
+    const int na = a0 < 8 ? 2 : 1;
+    uint4 raw[2][4], wq[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j >= na) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int h = hs + 16 * k;
+        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
+      }
+      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j >= na) break;
+      const int a = a0 + j;
+      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 cu = raw[j][k];
+        const int h = hs + 16 * k;
+        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
+          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
+          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
+          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 cs = rope[4 * chn + e];
+            const float x0 = x[2 * e], x1 = x[2 * e + 1];
+            x[2 * e] = x0 * cs.x - x1 * cs.y;
+            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+          }
+        }
+        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                   pack_f16x2(x[6], x[7]));
+        sts128(c.sb + SM_Q + a * 8192 + h * 128 + ((chn ^ (h & 7)) << 4), o);
+      }
+      if ((a & 1) == 1 || a == 8) {
+        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
+        fence_async_smem();
+        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
+      }
+    }
+  }
+  // per-head statistics: eight lanes hold the pieces of head hs + 16 k
+  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v = ss[k];
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    const int h = hs + 16 * k;
+    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
+  }
+  return grp.sync(c);
+}
+
 // ================================================================== SM
 // One row of the tile per thread (TMEM lane = row).  Softmax of tile g, then the
 // rotary part of the keys of the next tile, which QK^T needs after PV of tile g.
@@ -626,8 +786,10 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
   float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
   Group grp{B_SMG, 0};
+  const QArgs qa{P.q, P.norm_w, P.h_q, P.rms_eps, P.score_scale_log2};
   uint32_t g = 0, seq = 0, nq = 0;   // tiles, items, items with tiles
-  // next item with tiles: its info waited for and the rope of its tile 0 converted
+  // next item with tiles: its info waited for, its q~ built (once QK^T of the previous
+  // item has completed) and the rope of its tile 0 converted
   auto open_item = [&]() -> int {
     while (true) {
       const int b = seq % NB;
@@ -635,6 +797,8 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
+        if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
+        if (!build_q(qa, c, b, r, grp)) return -1;
         sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g);
         return c.misc[M_ABORT] ? -1 : 1;
       }
@@ -648,26 +812,18 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
     const int* info = item_info(c, b);
     const int T = info[IT_T], nrows = info[IT_NROWS];
     const uint32_t* list = item_list(P, b) + info[IT_ROW0];
-    // the per-head factor of the scores (scale * log2(e) / rms(q)), published with q~
+    // the next item's q into L2 when its info is already out
     {
-      const volatile int* qgen = reinterpret_cast<const volatile int*>(c.sm + SM_QGEN);
-      bool ok = true;
-      if (qgen[b] != (int)seq + 1) {
-        const unsigned long long start = clock64();
-        while (qgen[b] != (int)seq + 1) {
-          __nanosleep(200);
-          if (c.misc[M_ABORT]) { ok = false; break; }
-          if (clock64() - start > WAIT_LIMIT_CYCLES) {
-            atomicOr(c.status, DSA_STATUS_WAIT_TIMEOUT);
-            c.misc[M_ABORT] = 1;
-            ok = false;
-            break;
-          }
+      const int nb = (seq + 1) % NB;
+      if (__all_sync(0xFFFFFFFFu, mbar_try(bar(c, B_ITFULL + nb), ((seq + 1) / NB) & 1))) {
+        const int* ni = item_info(c, nb);
+        if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + (size_t)ni[IT_TOKEN] * P.h_q * D_QK);
+          for (int l = r; l < P.h_q * 9; l += N_SM) prefetch_line_l2(qn + 128 * l);
         }
       }
-      if (!__all_sync(0xFFFFFFFFu, ok)) return;
-      __threadfence_block();
     }
+    // the per-head factor of the scores (scale * log2(e) / rms(q)), written with q~
     const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
     if (r < 64) s_m[r] = -INFINITY;
     if (!grp.sync(c)) return;
@@ -801,100 +957,6 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
 }
 
 // ================================================================== EPI
-// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
-// operand of QK^T.  The per-head factor softmax_scale * log2(e) / rms(q) multiplies the
-// scores instead (the rotation and QK^T are linear in q~), so the statistics need not come
-// first.  64 heads x 9 atoms x 8 chunks of 8 dims: thread-piece j covers head
-// (er / 8) + 16 (j % 4), chunk er % 8, atom j / 4, so one warp reads four 128-byte head
-// rows and writes them with conflict-free swizzled stores.  Chunk c of the latent dims
-// (atoms 2c, 2c + 1) is announced on QRDY[c], the rotary atom on QRDY[4], so that QK^T
-// can start before the whole of q~ is written; the statistics follow.
-struct QArgs {
-  const uint16_t* q;
-  const uint16_t* norm_w;
-  int h_q;
-  float eps, c2;
-};
-
-DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, uint32_t seq, int er, Group& grp) {
-  const int* info = item_info(c, b);
-  const int t = info[IT_TOKEN];
-  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-  const int hs = er >> 3, chn = er & 7;
-  const uint16_t* qt = P.q + (size_t)t * P.h_q * D_QK;
-  float ss[4] = {0.f, 0.f, 0.f, 0.f};
-  // rounds of two atoms: eight q pieces (four heads x two atoms) and two norm-weight
-  // pieces in flight per thread
-#pragma unroll 1
-  for (int a0 = 0; a0 < 9; a0 += 2) {
-    const int na = a0 < 8 ? 2 : 1;
-    uint4 raw[2][4], wq[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j >= na) break;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int h = hs + 16 * k;
-        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
-      }
-      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j >= na) break;
-      const int a = a0 + j;
-      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 cu = raw[j][k];
-        const int h = hs + 16 * k;
-        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
-          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
-          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
-          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
-        }
-        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 cs = rope[4 * chn + e];
-            const float x0 = x[2 * e], x1 = x[2 * e + 1];
-            x[2 * e] = x0 * cs.x - x1 * cs.y;
-            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
-          }
-        }
-        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                   pack_f16x2(x[6], x[7]));
-        sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
-      }
-      if ((a & 1) == 1 || a == 8) {
-        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
-        fence_async_smem();
-        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
-      }
-    }
-  }
-  // per-head statistics: eight lanes hold the pieces of head hs + 16 k
-  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v = ss[k];
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    const int h = hs + 16 * k;
-    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
-  }
-  grp.sync(c);
-  if (er == 0) {
-    __threadfence_block();
-    reinterpret_cast<volatile int*>(c.sm + SM_QGEN)[b] = (int)seq + 1;
-  }
-}
-
 // The epilogue reads O^T out of TMEM one dim per lane, 16 heads at a time, and finishes
 // it from registers; each 64-head column block of TMEM is released as soon as it is read.
 DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int lane) {
@@ -905,9 +967,7 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
   const float ln2 = 0.69314718055994531f;
   const bool is_split = P.n_splits > 1;
   Group grp{B_EPG, 0};
-  const QArgs qa{P.q, P.norm_w, P.h_q, P.rms_eps, P.score_scale_log2};
   uint32_t nq = 0;   // items with tiles
-  int built = -1;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq % NB;
     if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return;
@@ -915,23 +975,6 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
     if (info[IT_ITEM] < 0) return;
     const int t = info[IT_TOKEN], split = info[IT_SPLIT], T = info[IT_T];
     if (T > 0) {
-      if (built != (int)seq) {
-        if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return;
-        build_q(qa, c, b, seq, er, grp);
-      }
-      // the next item's q~ as soon as this item's QK^T no longer reads the buffer
-      {
-        const int nb = (seq + 1) % NB;
-        if (!wait_bar_w(c, B_ITFULL + nb, ((seq + 1) / NB) & 1)) return;
-        const int* ninfo = item_info(c, nb);
-        if (ninfo[IT_ITEM] >= 0 && ninfo[IT_T] > 0) {
-          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + (size_t)ninfo[IT_TOKEN] * P.h_q * D_QK);
-          for (int l = er; l < P.h_q * 9; l += N_EPI) prefetch_line_l2(qn + 128 * l);
-          if (!wait_bar_w(c, B_QFREE, nq & 1)) return;
-          build_q(qa, c, nb, seq + 1, er, grp);
-          built = (int)seq + 1;
-        }
-      }
       if (!wait_bar_w(c, B_ODONE, nq & 1)) return;
       if (!wait_bar_w(c, B_MFIN, nq & 1)) return;
       tc_fence_after();
@@ -961,37 +1004,15 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       if (is_split && er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = s_else[er];
       const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-      float* part = is_split ? P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT : nullptr;
+      if (is_split) {
+        float* part = P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT;
 #pragma unroll 1
-      for (int cidx = 0; cidx < 4; ++cidx) {
-        const int d = 128 * cidx + 32 * e + lane;
-#pragma unroll 1
-        for (int hq = 0; hq < 4; ++hq) {
-          uint32_t a[16];
-          tmem_ld16(tmem + tlane + TM_O + 64 * cidx + 16 * hq, a);
-          tc_wait_ld();
-          if (hq == 3) {
-            tc_fence_before();
-            mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
-          }
-          const float4* il4 = reinterpret_cast<const float4*>(s_el + 16 * hq);
-          float v[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f = il4[q];
-            v[4 * q] = __uint_as_float(a[4 * q]) * f.x;
-            v[4 * q + 1] = __uint_as_float(a[4 * q + 1]) * f.y;
-            v[4 * q + 2] = __uint_as_float(a[4 * q + 2]) * f.z;
-            v[4 * q + 3] = __uint_as_float(a[4 * q + 3]) * f.w;
-          }
-          if (is_split) {
-            float* o = part + (size_t)(16 * hq) * D_LAT + d;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[(size_t)i * D_LAT] = v[i];
-          } else {
-            finalize_lanes(O, v, t, 16 * hq, d, lane, rope);
-          }
-        }
+        for (int cidx = 0; cidx < 4; ++cidx) epi_chunk<16>(c, tmem, e, lane, cidx, s_el, O, t, part, rope);
+      } else {
+        // column blocks 1 and 2 are finished by the dequant warps once 1/l is out
+        mbar_arrive(bar(c, B_LREADY));
+        epi_chunk<16>(c, tmem, e, lane, 0, s_el, O, t, nullptr, rope);
+        epi_chunk<16>(c, tmem, e, lane, 3, s_el, O, t, nullptr, rope);
       }
       ++nq;
     } else {
@@ -1124,16 +1145,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     mbar_init(bar(c, B_PFULL), N_SM);
     mbar_init(bar(c, B_PFREE), 1);
     mbar_init(bar(c, B_ODONE), 1);
-    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_EPI);
+    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_SM);
     mbar_init(bar(c, B_QFREE), 1);
     mbar_init(bar(c, B_MFIN), N_SM);
+    mbar_init(bar(c, B_LREADY), N_EPI);
     mbar_init(bar(c, B_SMG), N_SM);
     mbar_init(bar(c, B_EPG), N_EPI);
     mbar_init(bar(c, B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
     c.misc[M_LAST] = 0;
-    for (int i = 0; i < NB; ++i) reinterpret_cast<volatile int*>(c.sm + SM_QGEN)[i] = 0;
   }
   if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
   {
@@ -1147,7 +1168,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   const uint32_t tmem = (uint32_t)c.misc[M_TMEM];
 
   if (warp < W_SM) {
-    dq_role(P, c, warp, lane);
+    dq_role(P, c, tmem, warp, lane);
   } else if (warp < W_EPI) {
     sm_role(P, c, tmem, warp - W_SM, lane);
   } else if (warp < W_MMA) {
