@@ -90,7 +90,7 @@ enum {
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
-enum { M_TMEM = 0, M_ABORT, M_LAST, M_TOKEN };                   // misc ints
+enum { M_TMEM = 0, M_ABORT, M_COMBINE, M_TOKEN, M_SPLIT };         // misc ints
 enum { IT_ITEM = 0, IT_TOKEN, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS }; // item info ints
 
 struct KParams {
@@ -1034,25 +1034,26 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       }
     }
     if (is_split) {
-      // the last split of the token to arrive combines all partials after the CTA's roles
-      // have finished (one item per CTA on this path)
+      // this split's partial is out: it counts in, and after the CTA's roles have
+      // finished every split of the token combines one slice of it (one item per CTA on
+      // this path)
       __threadfence();
       if (!grp.sync(c)) return;
       if (er == 0) {
-        const uint32_t old = atomicAdd(&P.counters[t], 1u);
-        const int last = (old == (uint32_t)(P.n_splits - 1));
-        if (last) P.counters[t] = 0u;
-        c.misc[M_LAST] = last;
+        atomicAdd(&P.counters[t], 1u);
+        c.misc[M_COMBINE] = 1;
         c.misc[M_TOKEN] = t;
+        c.misc[M_SPLIT] = split;
       }
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
   }
 }
 
-// Combine of one token's split partials by the whole CTA: thread = (head, 32-dim block),
-// weights exp2(lse_s - M) / sum over splits.
-DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int tid) {
+// Combine of one token's split partials: split `part` of the token takes the slice
+// part / n_splits of its (head, 32-dim block) units, one unit per thread; weights
+// exp2(lse_s - M) / sum over splits.
+DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int part, int tid) {
   float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);       // [MAX_SPLITS][64]
   float* s_lse = s_cw + MAX_SPLITS * 64;                       // [64]
   float2* s_rope = reinterpret_cast<float2*>(s_lse + 64);      // [32] (cos, sin)
@@ -1073,7 +1074,7 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int tid) {
     s_lse[tid] = den > 0.f ? (M + log2f(den)) * ln2 : -INFINITY;
   }
   __syncthreads();
-  if (P.out_lse && tid < P.h_q) P.out_lse[(size_t)t * P.h_q + tid] = s_lse[tid];
+  if (part == 0 && P.out_lse && tid < P.h_q) P.out_lse[(size_t)t * P.h_q + tid] = s_lse[tid];
   // the rotary table of this token, rebuilt (the item buffers are gone)
   if (tid < 32) {
     const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[tid];
@@ -1084,7 +1085,8 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int tid) {
   }
   __syncthreads();
   const float2* rope = s_rope;
-  for (int u = tid; u < P.h_q * 16; u += NTHREADS) {
+  const int u0 = part * P.h_q * 16 / ns, u1 = (part + 1) * P.h_q * 16 / ns;
+  for (int u = u0 + tid; u < u1; u += NTHREADS) {
     const int h = u >> 4, blk = u & 15;
     float v[32];
 #pragma unroll
@@ -1154,7 +1156,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     mbar_init(bar(c, B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
-    c.misc[M_LAST] = 0;
+    c.misc[M_COMBINE] = 0;
   }
   if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
   {
@@ -1194,9 +1196,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
-  if (P.n_splits > 1 && c.misc[M_LAST] && !c.misc[M_ABORT]) {
-    __threadfence();
-    combine_token(P, c, c.misc[M_TOKEN], tid);
+  if (P.n_splits > 1 && c.misc[M_COMBINE] && !c.misc[M_ABORT]) {
+    // every split of the token has stored its partial (the splits are co-resident: this
+    // path is a cooperative launch); bounded wait on the token's arrival count
+    const int t = c.misc[M_TOKEN];
+    if (tid == 0) {
+      const volatile uint32_t* cnt = P.counters + t;
+      const unsigned long long start = clock64();
+      while (*cnt < (uint32_t)P.n_splits) {
+        __nanosleep(64);
+        if (clock64() - start > WAIT_LIMIT_CYCLES) {
+          atomicOr(c.status, DSA_STATUS_WAIT_TIMEOUT);
+          c.misc[M_ABORT] = 1;
+          break;
+        }
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    if (!c.misc[M_ABORT]) combine_token(P, c, t, c.misc[M_SPLIT], tid);
   }
 }
 
@@ -1340,7 +1358,19 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.n_items = p->s_q * ns;
   rope_turn_table(p->rope_base, K.rope_turns);
   const int grid = K.n_items < sms ? K.n_items : sms;
-  dsa_fwd_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(K);
+  // the split path waits across CTAs for the combine: a cooperative launch keeps its
+  // CTAs (one per item, at most one per SM) co-resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute coop[1];
+  coop[0].id = cudaLaunchAttributeCooperative;
+  coop[0].val.cooperative = 1;
+  cfg.attrs = coop;
+  cfg.numAttrs = ns > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, dsa_fwd_kernel, K) != cudaSuccess) return DSA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }
