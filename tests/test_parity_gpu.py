@@ -20,6 +20,9 @@ def _lib():
 
 def _full(w, **kw):
     g = parity.run_gpu(w, **kw)
+    # a bounded wait that ran out (or an index the kernel rejected) is reported as such,
+    # before any value comparison
+    assert g["status"] == 0 or kw.get("flags", 0), f"{w.name}: kernel status {g['status']:#x}"
     r = parity.run_oracle(w)
     return g, r, parity.compare(g, r, label=w.name)
 
@@ -49,6 +52,7 @@ def test_batched_decode_64():
 def test_full_size_workloads_sampled_tokens(name):
     w = W.make(name)
     g = parity.run_gpu(w)
+    assert g["status"] == 0, f"{name}: kernel status {g['status']:#x}"
     rng = np.random.default_rng(123)
     tok = np.unique(np.concatenate([[0, 1, 2, w.s_q - 1], rng.choice(w.s_q, size=40, replace=False)]))
     r = parity.run_oracle(parity.subset(w, tok))
