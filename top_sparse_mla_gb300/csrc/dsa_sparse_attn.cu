@@ -458,6 +458,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
   const int sub = lane >> 3, ch = lane & 7;
   const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
   const uint32_t c0 = (uint32_t)(2 * (ch & 3));
+  const uint32_t pa = c0 + (uint32_t)(ch >> 2), pb = c0 + 1 - (uint32_t)(ch >> 2);   // 16-byte chunks of the two stores
   uint4 raw[2][4];
   uint4 scl;
   DqRows cur, nxt;
@@ -534,13 +535,17 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float sv = __uint_as_float(__shfl_sync(0xFFFFFFFFu, sc, sub * 8 + k));
+          // lanes of the second 64-dim atom (ch >= 4) store their upper eight dims first:
+          // the eight lanes of a row then hit eight distinct 16-byte bank groups
+          const uint4 rw = raw[cidx & 1][k];
+          const uint4 rr = ch >= 4 ? make_uint4(rw.z, rw.w, rw.x, rw.y) : rw;
           uint32_t o[8];
-          dequant16(raw[cidx & 1][k], __float2half2_rn(sv), o);
+          dequant16(rr, __float2half2_rn(sv), o);
           const uint32_t row = (uint32_t)(16 * w + 4 * k + sub);
           const uint32_t rsw = row & 7;
           const uint32_t rb = cbase + (row >> 3) * 1024 + rsw * 128;
-          sts128(rb + ((c0 ^ rsw) << 4), make_uint4(o[0], o[1], o[2], o[3]));
-          sts128(rb + (((c0 + 1) ^ rsw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+          sts128(rb + ((pa ^ rsw) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+          sts128(rb + ((pb ^ rsw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
         }
         fence_async_smem();
         mbar_arrive(bar(c, B_VFULL + cidx));
