@@ -98,7 +98,12 @@ int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32
  * for invalid parameters. */
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
 
-/* The fused forward pass (steps 1-7). */
+/* The fused forward pass (steps 1-7).  It clears the workspace header with an async
+ * memset and launches one kernel on `stream`; both can be captured in a CUDA graph.
+ * When the tokens are few (dsa_sparse_attn_num_splits > 1) each CTA takes one
+ * (token, split) item and the launch is cooperative, so that the splits of a token can
+ * wait for one another before each combines its share of the partial outputs; the grid
+ * is then at most one CTA per SM. */
 int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp,
                         const int32_t* indices, const int32_t* topk_length,
                         const int32_t* positions, const void* norm_w,
