@@ -178,23 +178,6 @@ DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
 }
 DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 8 * b; }
 
-// Reduce 32 per-lane values across the warp, one result per value: afterwards lane L
-// holds the reduction of value L in v[0].
-template <bool IS_MAX>
-DSA_DEV void reduce32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int k = 16, n = 32; k >= 1; k >>= 1, n >>= 1) {
-    const bool upper = (lane & k) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, k);
-      v[i] = IS_MAX ? fmaxf(keep, recv) : keep + recv;
-    }
-  }
-}
-
 // ================================================================== PREP
 // Items, row lists and rotary tables, one item ahead of the other roles.
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
