@@ -25,8 +25,11 @@
 //                      rotary table; up to three items ahead
 //
 // TMEM: O^T 0..255, l 256..319, S^T 320..447 (two buffers), K~ rope part 448..511 (two).
-// Every mbarrier wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT,
-// every role leaves its loop, the tensor core is drained and TMEM freed.
+// With few tokens each token's rows are split over several CTAs, one item per CTA, and
+// the launch is cooperative: once its roles are done, every split of a token waits for
+// the others and combines its share of the fp32 partial outputs.
+// Every wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT, every role
+// leaves its loop, the tensor core is drained and TMEM freed.
 
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
