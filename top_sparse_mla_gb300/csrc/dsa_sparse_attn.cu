@@ -234,7 +234,8 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
         const int j = base + 32 * k + lane;
         v[k] = (j < L) ? __ldg(irow + j) : -1;
       }
-#pragma unroll
+      // (not unrolled: the code of all roles shares the SM's instruction caches)
+#pragma unroll 1
       for (int k = 0; k < 16; ++k) {
         const int j = base + 32 * k + lane;
         const bool cmp = j >= P.n_swa_cols;
@@ -604,7 +605,9 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
       const uint32_t sb = g & 1;
       const uint32_t d_s = tmem + TM_S + 64 * sb;
       if (!wait_bar(c, B_SFREE + sb, ((g >> 1) & 1) ^ 1)) return;
-#pragma unroll
+      // chunk loop not unrolled: a smaller issue loop misses the instruction caches less,
+      // which the one issuing thread would otherwise stall on
+#pragma unroll 1
       for (int cidx = 0; cidx < 4; ++cidx) {
         // q~ chunk (first tile of an item) and the latent chunk of this tile
         if (tt == 0 && !wait_bar(c, B_QRDY + cidx, nq & 1)) return;
@@ -630,7 +633,7 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
       if (!wait_bar(c, B_PFULL, g & 1)) return;
       tc_fence_after();
       const uint32_t first = tt == 0 ? 0u : 1u;
-#pragma unroll
+#pragma unroll 1
       for (int cidx = 0; cidx < 4; ++cidx) {
         if (tt == 0 && nq > 0) {
           // the previous item's epilogue has read this part of O^T (and l)
@@ -995,16 +998,14 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       if (is_split && er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = s_else[er];
       const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-      if (is_split) {
-        float* part = P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT;
+      // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
+      // is out; one call site for the blocks keeps the finish code in one copy
+      if (!is_split) mbar_arrive(bar(c, B_LREADY));
+      float* part = is_split ? P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT : nullptr;
+      const int nblk = is_split ? 4 : 2;
 #pragma unroll 1
-        for (int cidx = 0; cidx < 4; ++cidx) epi_chunk<16>(c, tmem, e, lane, cidx, s_el, O, t, part, rope);
-      } else {
-        // column blocks 1 and 2 are finished by the dequant warps once 1/l is out
-        mbar_arrive(bar(c, B_LREADY));
-        epi_chunk<16>(c, tmem, e, lane, 0, s_el, O, t, nullptr, rope);
-        epi_chunk<16>(c, tmem, e, lane, 3, s_el, O, t, nullptr, rope);
-      }
+      for (int bi = 0; bi < nblk; ++bi)
+        epi_chunk<16>(c, tmem, e, lane, is_split ? bi : 3 * bi, s_el, O, t, part, rope);
       ++nq;
     } else {
       // no valid column: o = 0, scale codes 0, LSE -inf
