@@ -137,21 +137,27 @@ constexpr unsigned long long WAIT_LIMIT_CYCLES = 4000000000ull;   // ~2 s at 2 G
 
 DSA_DEV uint32_t bar(const Ctx& c, int i) { return c.sb + SM_BAR + 8u * (uint32_t)i; }
 
-// Bounded wait: false when the limit passes (raising the abort flag and the status bit)
-// or when another thread of the CTA has already aborted.
-DSA_DEV bool wait_bar(const Ctx& c, int b, uint32_t parity) {
-  const uint32_t addr = bar(c, b);
-  if (mbar_try(addr, parity)) return true;
+// The waiting part of a bounded wait, out of line: one copy serves every wait site (the
+// code of all roles shares the SM's instruction caches).  False when the limit passes
+// (raising the abort flag and the status bit) or when another thread of the CTA has
+// already aborted.
+__device__ __noinline__ bool wait_slow(uint32_t addr, uint32_t parity, volatile int* misc, uint32_t* status) {
   const unsigned long long start = clock64();
   while (true) {
     if (mbar_wait_susp(addr, parity)) return true;
-    if (c.misc[M_ABORT]) return false;
+    if (misc[M_ABORT]) return false;
     if (clock64() - start > WAIT_LIMIT_CYCLES) {
-      atomicOr(c.status, DSA_STATUS_WAIT_TIMEOUT);
-      c.misc[M_ABORT] = 1;
+      atomicOr(status, DSA_STATUS_WAIT_TIMEOUT);
+      misc[M_ABORT] = 1;
       return false;
     }
   }
+}
+// Bounded wait: one try inline, the rest out of line.
+DSA_DEV bool wait_bar(const Ctx& c, int b, uint32_t parity) {
+  const uint32_t addr = bar(c, b);
+  if (mbar_try(addr, parity)) return true;
+  return wait_slow(addr, parity, c.misc, c.status);
 }
 // Warp-collective form: the warp agrees on the outcome, so it never splits before a
 // full-warp shuffle or TMEM access.
