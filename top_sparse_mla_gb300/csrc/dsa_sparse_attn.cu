@@ -6,16 +6,17 @@
 // Work item = (query token, KV split).  One CTA of 18 warps per SM; the warps are
 // specialised and talk through mbarriers:
 //
-//   DQ   (warps 0-7)   gathered rows -> fp16 latent tile [128 rows x 512 dims] in shared
-//                      memory, fp32 block scale folded in.  The one tile is the A operand
-//                      of both contractions: K-major for QK^T (M = rows), MN-major for PV
-//                      (M = dims).  Raw bytes are loaded two chunks ahead, rows are
-//                      prefetched into L2 one tile ahead.  Between items (no splits): the
-//                      MXFP8 finish of output dims 128..383 of the previous item.
-//   SM   (warps 8-11)  when an item opens: q~ = RoPE(q * w) in fp16 as the B operand of
-//                      QK^T, chunk by chunk, and the fp32 RMS statistics of q; then per
-//                      tile the softmax over S^T (lazy running max, exp2, fp16 P) with the
-//                      per-head factor softmax_scale * log2(e) / rms(q), and the rotary
+//   DQ   (warps 0-7)   when an item opens (right after the previous item's last QK^T):
+//                      q~ = RoPE(q * w) in fp16 as the B operand of QK^T, chunk by chunk,
+//                      and the fp32 RMS statistics of q.  Per tile: gathered rows -> fp16
+//                      latent tile [128 rows x 512 dims] in shared memory, fp32 block scale
+//                      folded in.  The one tile is the A operand of both contractions:
+//                      K-major for QK^T (M = rows), MN-major for PV (M = dims).  Raw bytes
+//                      are loaded two chunks ahead, rows are prefetched into L2 one tile
+//                      ahead.  Between items (no splits): the MXFP8 finish of output dims
+//                      128..383 of the previous item.
+//   SM   (warps 8-11)  per tile the softmax over S^T (lazy running max, exp2, fp16 P) with
+//                      the per-head factor softmax_scale * log2(e) / rms(q), and the rotary
 //                      part of the next tile's keys (bf16 -> fp16) into TMEM
 //   EPI  (warps 12-15) 1/l and the LSE; the epilogue: O^T / l out of TMEM into the global
 //                      output (dims 0..127 and 384..511, or all of it as a split partial)
@@ -89,7 +90,7 @@ enum {
   B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
   B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
   B_ITFULL, B_ITEMPTY = B_ITFULL + NB, B_ODONE = B_ITEMPTY + NB, B_OFREE,
-  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_MFIN, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_COUNT
+  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_COUNT
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
@@ -412,6 +413,93 @@ DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, 
   }
 }
 
+// ================================================================== q~
+// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
+// operand of QK^T, built by the 256 dequant threads.  The per-head factor
+// softmax_scale * log2(e) / rms(q) multiplies the scores instead (the rotation and QK^T
+// are linear in q~), so the statistics need not come first.  64 heads x 9 atoms x 8
+// chunks of 8 dims: thread-piece j covers head (er / 8) + 32 (j % 2), chunk er % 8, atom
+// j / 2, so one warp reads four 128-byte head rows and writes them with conflict-free
+// swizzled stores.  Chunk c of the latent dims (atoms 2c, 2c + 1) is announced on
+// QRDY[c], the rotary atom on QRDY[4], so that QK^T can start before the whole of q~ is
+// written; the statistics follow on QSTAT[b].
+struct QArgs {
+  const uint16_t* q;
+  const uint16_t* norm_w;
+  int h_q;
+  float eps, c2;
+};
+
+DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
+  const uint16_t* qt = P.q + (size_t)item_info(c, b)[IT_TOKEN] * P.h_q * D_QK;
+  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  const int hs = er >> 3, chn = er & 7;
+  float ss[2] = {0.f, 0.f};
+  // rounds of three atoms: six q pieces (two heads x three atoms) and three norm-weight
+  // pieces in flight per thread
+#pragma unroll 1
+  for (int a0 = 0; a0 < 9; a0 += 3) {
+    uint4 raw[3][2], wq[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int h = hs + 32 * k;
+        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
+      }
+      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int a = a0 + j;
+      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint4 cu = raw[j][k];
+        const int h = hs + 32 * k;
+        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
+          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
+          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
+          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 cs = rope[4 * chn + e];
+            const float x0 = x[2 * e], x1 = x[2 * e + 1];
+            x[2 * e] = x0 * cs.x - x1 * cs.y;
+            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+          }
+        }
+        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                   pack_f16x2(x[6], x[7]));
+        sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
+      }
+      if ((a & 1) == 1 || a == 8) {
+        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
+        fence_async_smem();
+        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
+      }
+    }
+  }
+  // per-head statistics: eight lanes hold the pieces of head hs + 32 k
+  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    float v = ss[k];
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    const int h = hs + 32 * k;
+    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
+  }
+  mbar_arrive(bar(c, B_QSTAT + b));
+}
+
 // ================================================================== DQ
 // Lane (sub, ch) of warp w converts 16 bytes (16 dims) of rows 16 w + 4 k + sub,
 // k = 0..3, per 128-dim chunk: eight lanes read 128 contiguous bytes of a row.  The
@@ -477,8 +565,9 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
     pend = -1;
     return true;
   };
-  // next item with tiles: its info waited for, rows of tile 0 and its first two chunks
-  // in flight
+  const QArgs qa{P.q, P.norm_w, P.h_q, P.rms_eps, P.score_scale_log2};
+  // next item with tiles: its info waited for, its q~ built (once QK^T of the previous
+  // item has completed), rows of tile 0 and its first two chunks in flight
   auto open_item = [&]() -> int {   // 1 = opened, 0 = no more items, -1 = aborted
     while (true) {
       const int b = seq % NB;
@@ -486,12 +575,15 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
+        if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
+        build_q(qa, c, b, 32 * w + lane);
         dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, ch, cur);
         scl = dq_load_scales(P, cur);
         dq_load_chunk(P, raw[0], 0, cur, ch);
         dq_load_chunk(P, raw[1], 1, cur, ch);
         return 1;
       }
+      mbar_arrive(bar(c, B_QSTAT + b));   // no q~: the phase still follows the buffer's uses
       mbar_arrive(bar(c, B_ITEMPTY + b));
       ++seq;
     }
@@ -662,95 +754,6 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   }
 }
 
-// ================================================================== q~
-// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
-// operand of QK^T.  The per-head factor softmax_scale * log2(e) / rms(q) multiplies the
-// scores instead (the rotation and QK^T are linear in q~), so the statistics need not come
-// first.  64 heads x 9 atoms x 8 chunks of 8 dims: thread-piece j covers head
-// (er / 8) + 16 (j % 4), chunk er % 8, atom j / 4, so one warp reads four 128-byte head
-// rows and writes them with conflict-free swizzled stores.  Chunk c of the latent dims
-// (atoms 2c, 2c + 1) is announced on QRDY[c], the rotary atom on QRDY[4], so that QK^T
-// can start before the whole of q~ is written; the statistics follow.
-struct QArgs {
-  const uint16_t* q;
-  const uint16_t* norm_w;
-  int h_q;
-  float eps, c2;
-};
-
-DSA_DEV bool build_q(const QArgs& P, const Ctx& c, int b, int er, Group& grp) {
-  const uint16_t* qt = P.q + (size_t)item_info(c, b)[IT_TOKEN] * P.h_q * D_QK;
-  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-  const int hs = er >> 3, chn = er & 7;
-  float ss[4] = {0.f, 0.f, 0.f, 0.f};
-  // rounds of two atoms: eight q pieces (four heads x two atoms) and two norm-weight
-  // pieces in flight per thread
-#pragma unroll 1
-  for (int a0 = 0; a0 < 9; a0 += 2) {
-    const int na = a0 < 8 ? 2 : 1;
-    uint4 raw[2][4], wq[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j >= na) break;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int h = hs + 16 * k;
-        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
-      }
-      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j >= na) break;
-      const int a = a0 + j;
-      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 cu = raw[j][k];
-        const int h = hs + 16 * k;
-        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
-          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
-          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
-          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
-        }
-        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 cs = rope[4 * chn + e];
-            const float x0 = x[2 * e], x1 = x[2 * e + 1];
-            x[2 * e] = x0 * cs.x - x1 * cs.y;
-            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
-          }
-        }
-        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                   pack_f16x2(x[6], x[7]));
-        sts128(c.sb + SM_Q + a * 8192 + h * 128 + ((chn ^ (h & 7)) << 4), o);
-      }
-      if ((a & 1) == 1 || a == 8) {
-        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
-        fence_async_smem();
-        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
-      }
-    }
-  }
-  // per-head statistics: eight lanes hold the pieces of head hs + 16 k
-  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v = ss[k];
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    const int h = hs + 16 * k;
-    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
-  }
-  return grp.sync(c);
-}
-
 // ================================================================== SM
 // One row of the tile per thread (TMEM lane = row).  Softmax of tile g, then the
 // rotary part of the keys of the next tile, which QK^T needs after PV of tile g.
@@ -786,7 +789,6 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
   float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
   Group grp{B_SMG, 0};
-  const QArgs qa{P.q, P.norm_w, P.h_q, P.rms_eps, P.score_scale_log2};
   uint32_t g = 0, seq = 0, nq = 0;   // tiles, items, items with tiles
   // next item with tiles: its info waited for, its q~ built (once QK^T of the previous
   // item has completed) and the rope of its tile 0 converted
@@ -797,8 +799,6 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
-        if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
-        if (!build_q(qa, c, b, r, grp)) return -1;
         sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g);
         return c.misc[M_ABORT] ? -1 : 1;
       }
@@ -823,7 +823,9 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         }
       }
     }
-    // the per-head factor of the scores (scale * log2(e) / rms(q)), written with q~
+    // the per-head factor of the scores (scale * log2(e) / rms(q)), written with q~ (one
+    // phase of QSTAT[b] per use of item buffer b: the next needs this buffer released)
+    if (!wait_bar_w(c, B_QSTAT + b, (seq / NB) & 1)) return;
     const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
     if (r < 64) s_m[r] = -INFINITY;
     if (!grp.sync(c)) return;
@@ -1145,7 +1147,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     mbar_init(bar(c, B_PFULL), N_SM);
     mbar_init(bar(c, B_PFREE), 1);
     mbar_init(bar(c, B_ODONE), 1);
-    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_SM);
+    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_DQ);
+    for (int i = 0; i < NB; ++i) mbar_init(bar(c, B_QSTAT + i), N_DQ);
     mbar_init(bar(c, B_QFREE), 1);
     mbar_init(bar(c, B_MFIN), N_SM);
     mbar_init(bar(c, B_LREADY), N_EPI);
