@@ -64,6 +64,15 @@ extern "C" {
 #define DSA_ERR_SCRATCH_LIMIT (-6)       /* shape needs more than DSA_NOALLOC_SCRATCH_BYTES */
 
 #define DSA_FLAG_CHECK_INDICES 1u        /* bounds-check every index against its pool */
+/* For tests of the failure path only: in CTA 0 the warp that publishes items first waits
+ * on an on-chip barrier that nothing completes.  That wait runs out after its bound
+ * (about 2 s), the CTA sets DSA_STATUS_WAIT_TIMEOUT, and every role of the CTA stops,
+ * drains the tensor core and frees its tensor memory, so the context stays usable.
+ * Without splits CTA 0 takes no item, and the other CTAs compute every output.  With
+ * splits (dsa_sparse_attn_num_splits > 1) token 0's first split is never computed:
+ * its other splits give up their bounded wait for it (also DSA_STATUS_WAIT_TIMEOUT),
+ * so token 0's output is left unwritten, and the other tokens are complete. */
+#define DSA_FLAG_TEST_WAIT_TIMEOUT 2u
 
 #define DSA_STATUS_INDEX_OUT_OF_RANGE 1u /* an index was >= its pool size (with the flag) */
 #define DSA_STATUS_WAIT_TIMEOUT 2u       /* an on-chip pipeline wait gave up; output invalid */

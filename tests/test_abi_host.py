@@ -38,6 +38,25 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"missing export {name}"
 
 
+def test_header_constants_match_the_binding():
+    # "#define NAME 2u", "#define NAME (-1)" and "#define NAME (24u << 20)"
+    pattern = re.compile(r"^#define (DSA_[A-Z0-9_]+) \(?(-?[0-9]+)u?(?: << ([0-9]+))?", re.M)
+    defines = {name: int(v) << int(shift or 0) for name, v, shift in pattern.findall(open(HEADER).read())}
+    assert "DSA_FLAG_TEST_WAIT_TIMEOUT" in defines and "DSA_STATUS_WAIT_TIMEOUT" in defines
+    for name, value in defines.items():
+        assert getattr(native, name) == value, name
+
+
+def test_flag_mask(lib):
+    # both defined flags pass the argument check (num_splits returns 0 on a bad argument)
+    p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096,
+                               flags=native.DSA_FLAG_CHECK_INDICES | native.DSA_FLAG_TEST_WAIT_TIMEOUT)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 8
+    for bad in (4, 8, 1 << 31):
+        p.flags = bad
+        assert native.dsa_sparse_attn_num_splits(p, 152) == 0
+
+
 def test_params_init_defaults(lib):
     p = native.dsa_params_init(4, 64, 640, 128, 1000, 2000)
     assert (p.s_q, p.h_q, p.topk, p.n_swa_cols, p.n_swa_rows, p.n_cmp_rows) == (4, 64, 640, 128, 1000, 2000)

@@ -90,7 +90,7 @@ enum {
   B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
   B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
   B_ITFULL, B_ITEMPTY = B_ITFULL + NB, B_ODONE = B_ITEMPTY + NB, B_OFREE,
-  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_COUNT
+  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_NEVER, B_COUNT
 };
 static_assert(B_COUNT <= 48, "barrier area");
 
@@ -205,6 +205,11 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     }
     return item;
   };
+  if ((P.flags & DSA_FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0) {
+    // test of the failure path: a wait that runs out, before this CTA takes an item
+    wait_slow(bar(c, B_NEVER), 0, c.misc, c.status);
+    return;
+  }
   int next = fetch(0);
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq % NB;
@@ -1155,6 +1160,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     mbar_init(bar(c, B_SMG), N_SM);
     mbar_init(bar(c, B_EPG), N_EPI);
     mbar_init(bar(c, B_DRAIN), 1);
+    mbar_init(bar(c, B_NEVER), 1);   // nothing arrives: the failure-path test waits on it
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     c.misc[M_ABORT] = 0;
     c.misc[M_COMBINE] = 0;
@@ -1273,7 +1279,7 @@ static int check_params(const dsa_params* p) {
   if (p->topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
   if (!(p->softmax_scale == p->softmax_scale) || !(p->rope_base > 0.f) || !(p->rms_eps >= 0.f))
     return DSA_ERR_INVALID_ARG;
-  if (p->flags & ~DSA_FLAG_CHECK_INDICES) return DSA_ERR_INVALID_ARG;
+  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT)) return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
 

@@ -21,6 +21,7 @@ DSA_ERR_CUDA = -4
 DSA_ERR_UNSUPPORTED_DEVICE = -5
 DSA_ERR_SCRATCH_LIMIT = -6
 DSA_FLAG_CHECK_INDICES = 1
+DSA_FLAG_TEST_WAIT_TIMEOUT = 2
 DSA_STATUS_INDEX_OUT_OF_RANGE = 1
 DSA_STATUS_WAIT_TIMEOUT = 2
 DSA_MAX_HEADS = 64
