@@ -54,6 +54,15 @@ def algorithmic_flops(w) -> int:
     return int(W.n_valid_rows(w).sum()) * (2 * w.h_q * 576 + 2 * w.h_q * 512)
 
 
+def kernels_per_call(params) -> int:
+    """Kernels one forward call launches: the fused kernel, preceded on the queue path
+    (no token split, at most 65536 tokens) by the kernel that orders the queue.  The split
+    path clears its workspace with a memset instead."""
+    from top_sparse_mla_gb300 import native
+    queue = native.dsa_sparse_attn_num_splits(params, 0) == 1
+    return 2 if queue and params.s_q <= 65536 else 1
+
+
 def profiled_traffic(workload_name: str):
     """DRAM bytes per launch (read + write) from the committed ncu summary of this
     workload, or None when the summary is missing or was taken on other kernel source
@@ -352,7 +361,7 @@ def run_native(args):
                          "alg_bytes_per_launch": b_alg},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * kernels_per_call(inp.params),
             "clocks": clocks,
             "per_config": per_config,
         }

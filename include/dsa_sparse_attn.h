@@ -37,8 +37,8 @@
  *               a token with no valid column (debug entry only; may be NULL)
  *
  * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream),
- * allocate nothing, and launch one kernel after one small memset of the workspace
- * header.  Arguments are checked on the host before anything is enqueued; a non-zero
+ * allocate nothing, and enqueue at most two kernels and one small memset (below).
+ * Arguments are checked on the host before anything is enqueued; a non-zero
  * return means nothing was enqueued (DSA_ERR_CUDA: the launch itself failed).
  * An index >= its pool's row count is undefined behaviour unless
  * DSA_FLAG_CHECK_INDICES is set; then that column is skipped and the device status
@@ -101,18 +101,26 @@ int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32
                     int64_t n_swa_rows, int64_t n_cmp_rows);
 
 /* Bytes of device workspace the forward call needs for `p` on a GPU with `num_sms`
- * SMs (num_sms <= 0: the current device).  The workspace holds a status word, one
- * combine counter per token, the compacted row lists of every CTA and, when a token's
- * rows are split across several CTAs, the per-split partial outputs.  0 is returned
- * for invalid parameters. */
+ * SMs (num_sms <= 0: the current device).  The workspace holds a status word and a
+ * queue head, one int32 per token (a combine counter on the split path, the queue's
+ * token order otherwise), the compacted row lists of every CTA and, when a token's rows
+ * are split across several CTAs, the per-split partial outputs.  0 is returned for
+ * invalid parameters. */
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
 
-/* The fused forward pass (steps 1-7).  It clears the workspace header with an async
- * memset and launches one kernel on `stream`; both can be captured in a CUDA graph.
- * When the tokens are few (dsa_sparse_attn_num_splits > 1) each CTA takes one
- * (token, split) item and the launch is cooperative, so that the splits of a token can
- * wait for one another before each combines its share of the partial outputs; the grid
- * is then at most one CTA per SM. */
+/* The fused forward pass (steps 1-7), enqueued on `stream`; everything it enqueues can
+ * be captured in a CUDA graph.
+ * - When the tokens are few (dsa_sparse_attn_num_splits > 1), each CTA takes one
+ *   (token, split) item. The call clears the workspace header and the combine counters
+ *   with an async memset. The fused kernel's launch is then cooperative, so that the
+ *   splits of a token can wait for one another before each combines its share of the
+ *   partial outputs; the grid is at most one CTA per SM.
+ * - Otherwise the CTAs (at most one per SM) take tokens from one queue. With at most
+ *   65536 tokens, a one-CTA kernel first clears the header and orders the queue: tokens
+ *   with the most 128-row tiles (from topk_length) come first, equal counts in token
+ *   order. The fused kernel is launched as its programmatic dependent. Above 65536
+ *   tokens a memset clears the header and tokens go in index order.
+ * The order decides which CTA computes a token, never the token's result. */
 int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp,
                         const int32_t* indices, const int32_t* topk_length,
                         const int32_t* positions, const void* norm_w,

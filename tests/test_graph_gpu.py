@@ -1,9 +1,10 @@
 """The forward call captured in a CUDA graph and replayed, against the same call made
 directly (C ABI through the binding).
 
-The call clears its workspace header with an asynchronous memset and then launches the
-kernel on the caller's stream, both capturable.  The single-token case takes the split
-path, whose launch is cooperative; the tiny case takes the queue path.
+The single-token case takes the split path: an asynchronous memset of the workspace
+header and counters, then the fused kernel's cooperative launch. The tiny case takes
+the queue path: the one-CTA order kernel, then the fused kernel as its programmatic
+dependent. Both sequences are captured on the caller's stream.
 """
 
 import numpy as np

@@ -111,10 +111,12 @@ struct KParams {
   float* out_lse;
   float* part_o;        // split partials [s_q][n_splits][64 heads][512 dims]
   float* part_lse;      // [s_q][n_splits][64] (log2 units)
-  uint32_t* counters;   // [s_q] split arrivals
+  uint32_t* counters;   // [s_q] split arrivals (split path)
+  const int32_t* order; // [s_q] tokens, most tiles first (queue path; shares the counters'
+                        // region), or null: tokens in order
   uint32_t* status;
   uint32_t* work;       // global item queue head
-  uint32_t* lists;      // [grid][2][DSA_MAX_TOPK] compacted row lists (bit 31: compressed pool)
+  uint32_t* lists;      // [grid][NB][DSA_MAX_TOPK] compacted row lists (bit 31: compressed pool)
   int s_q, h_q, topk, n_swa_cols;
   long long n_swa_rows, n_cmp_rows;
   float score_scale_log2;   // softmax_scale * log2(e)
@@ -195,13 +197,16 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   const bool split_path = P.n_splits > 1;
   // split path: exactly one item per CTA (the grid has one CTA per item), so the last
   // split of a token can run its combine with the whole CTA afterwards.  Otherwise items
-  // come from the global queue, each fetched one iteration before it is used.
+  // come from the global queue in the order of P.order (tokens with the most tiles
+  // first, so that the last items handed out are short ones), each fetched one iteration
+  // before it is used.
   auto fetch = [&](uint32_t seq) -> int {
     int item = 0;
     if (lane == 0) {
       if (split_path) item = seq == 0 ? (int)blockIdx.x : P.n_items;
       else item = (int)atomicAdd(P.work, 1u);
       item = item < P.n_items ? item : -1;
+      if (!split_path && item >= 0 && P.order) item = P.order[item];
     }
     return item;
   };
@@ -1121,6 +1126,71 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int part, int 
 }
 
 // ================================================================== the kernel
+// Queue path, before the fused kernel: clears the workspace header (status word, queue
+// head) and writes the order in which the queue hands out tokens, those with the most
+// 128-row tiles first.  With items of mixed length taken from one queue, the CTAs that
+// draw long items last finish late; longest-first leaves only short items for the end.
+// The tile count comes from topk_length alone (sentinels are not counted).  A stable
+// counting sort over the 17 possible tile counts: tokens of equal count keep their
+// order.  Each warp counts equal keys with one match, so a batch of equal lengths costs
+// one shared-memory atomic per warp.  The fused kernel is launched as this grid's
+// programmatic dependent: it may start its prologue at once, and it waits for this
+// grid's writes before it takes an item.
+constexpr int ORDER_THREADS = 1024;
+constexpr int ORDER_MAX_TOKENS = 65536;   // beyond this the queue takes tokens in order
+__global__ void __launch_bounds__(ORDER_THREADS, 1) dsa_order_kernel(const int32_t* __restrict__ topk_length,
+                                                                     int s_q, int topk, uint32_t* header,
+                                                                     int32_t* order) {
+  constexpr int NK = DSA_MAX_TOPK / TILE + 1, NW = ORDER_THREADS / 32;
+  __shared__ int s_next[NK];      // first free slot of each tile count
+  __shared__ int s_cnt[NW][NK];   // per warp: tokens of each count in the current chunk
+  __shared__ int s_off[NW][NK];   // per warp: where those tokens go
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  auto key = [&](int t) {
+    if (t >= s_q) return -1;
+    const int len = min(max(topk_length[t], 0), topk);
+    return (len + TILE - 1) / TILE;
+  };
+  if (tid < NK) s_next[tid] = 0;
+  for (int i = tid; i < NW * NK; i += ORDER_THREADS) (&s_cnt[0][0])[i] = 0;
+  if (tid < 64) header[tid] = 0;   // the 256-byte header: status word, queue head
+  __syncthreads();
+  for (int c0 = 0; c0 < s_q; c0 += ORDER_THREADS) {
+    const int k = key(c0 + tid);
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, k);
+    if (k >= 0 && (same & lt) == 0) atomicAdd(&s_next[k], __popc(same));
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int k = NK - 1; k >= 0; --k) {
+      const int n = s_next[k];
+      s_next[k] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < s_q; c0 += ORDER_THREADS) {
+    const int t = c0 + tid, k = key(t);
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, k);
+    if (k >= 0 && (same & lt) == 0) s_cnt[w][k] = __popc(same);
+    __syncthreads();
+    if (tid < NK) {   // one thread per count: the warps' slots in warp order
+      int run = s_next[tid];
+      for (int j = 0; j < NW; ++j) {
+        s_off[j][tid] = run;
+        run += s_cnt[j][tid];
+        s_cnt[j][tid] = 0;
+      }
+      s_next[tid] = run;
+    }
+    __syncthreads();
+    if (k >= 0) order[s_off[w][k] + __popc(same & lt)] = t;
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
@@ -1175,6 +1245,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)c.misc[M_TMEM];
+  // launched as the order kernel's programmatic dependent (queue path): its header and
+  // order are visible after this; a no-op for a launch without that dependency
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < W_SM) {
     dq_role(P, c, tmem, warp, lane);
@@ -1332,7 +1405,17 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   }
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
-  if (cudaMemsetAsync(ws, 0, L.counters_off + 4 * (size_t)p->s_q, st) != cudaSuccess) return DSA_ERR_CUDA;
+  const bool ordered = ns == 1 && p->s_q <= ORDER_MAX_TOKENS;
+  if (ordered) {
+    // header and the queue's order (in the counters' region, which the queue path does not use)
+    dsa_order_kernel<<<1, ORDER_THREADS, 0, st>>>(topk_length, p->s_q, p->topk, (uint32_t*)ws,
+                                                  (int32_t*)(ws + L.counters_off));
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  } else {
+    // header and the split arrival counters
+    const size_t n = ns > 1 ? L.counters_off + 4 * (size_t)p->s_q : L.counters_off;
+    if (cudaMemsetAsync(ws, 0, n, st) != cudaSuccess) return DSA_ERR_CUDA;
+  }
 
   KParams K;
   K.q = (const uint16_t*)q;
@@ -1349,6 +1432,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.part_o = ns > 1 ? (float*)(ws + L.part_o_off) : nullptr;
   K.part_lse = ns > 1 ? (float*)(ws + L.part_lse_off) : nullptr;
   K.counters = (uint32_t*)(ws + L.counters_off);
+  K.order = ordered ? (const int32_t*)(ws + L.counters_off) : nullptr;
   K.status = (uint32_t*)(ws + L.status_off);
   K.work = (uint32_t*)(ws + L.work_off);
   K.lists = (uint32_t*)(ws + L.lists_off);
@@ -1365,18 +1449,24 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.n_items = p->s_q * ns;
   rope_turn_table(p->rope_base, K.rope_turns);
   const int grid = K.n_items < sms ? K.n_items : sms;
-  // the split path waits across CTAs for the combine: a cooperative launch keeps its
-  // CTAs (one per item, at most one per SM) co-resident
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute coop[1];
-  coop[0].id = cudaLaunchAttributeCooperative;
-  coop[0].val.cooperative = 1;
-  cfg.attrs = coop;
-  cfg.numAttrs = ns > 1 ? 1 : 0;
+  // the split path waits across CTAs for the combine: a cooperative launch keeps its
+  // CTAs (one per item, at most one per SM) co-resident.  The ordered queue path starts
+  // while the order kernel runs, as its programmatic dependent.
+  cudaLaunchAttribute attr[1];
+  if (ns > 1) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (ns > 1 || ordered) ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, dsa_fwd_kernel, K) != cudaSuccess) return DSA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
