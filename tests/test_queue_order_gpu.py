@@ -8,10 +8,12 @@ its 256-byte header, in the region the split path uses for its arrival counters.
 65536 tokens the queue takes tokens in index order and no order is written.
 
 The order decides only which CTA computes a token, never the token's result. These
-tests check three things:
+tests check:
   * the order itself: a permutation, longest first and stable;
   * that every token is computed exactly once, on both sides of the 65536-token bound;
-  * that a token and its twin, given the same inputs, get bit-identical outputs.
+  * that a token and its twin, given the same inputs, get bit-identical outputs;
+  * that tokens without a valid column, placed among long ones, are written by the
+    queue path without stalling it.
 """
 
 import numpy as np
@@ -104,3 +106,20 @@ def test_every_token_once_at_the_order_bound(s_q):
         assert np.array_equal(g[k], g[k][twin], equal_nan=True), k
     # and the first 64 match the oracle
     parity.compare(g, parity.run_oracle(base), tokens=np.arange(64), label=f"repeated {s_q}")
+
+
+def test_tokens_without_rows_among_long_ones():
+    # Queue path. Two of every five tokens have only sentinels but a full topk_length:
+    # they have no tile, yet the order puts them among the longest tokens. Each CTA
+    # therefore meets items without tiles right after items with tiles, twice in a
+    # row. The epilogue share of the item before must not wait for items the queue has
+    # not handed out yet.
+    w = W.random_case(505, s_q=2000, h_q=8, n_swa_cols=64, n_cmp_cols=192, n_swa_rows=2048, n_cmp_rows=8192,
+                      n_sentinels=3)
+    t = np.arange(w.s_q)
+    w.indices[(t % 5 == 1) | (t % 5 == 2)] = -1
+    _, order = _run(w)
+    assert np.array_equal(order, np.argsort(-_tiles(w), kind="stable"))
+    g = parity.run_gpu(w)
+    assert g["status"] == 0
+    parity.compare(g, parity.run_oracle(w), label="empty tokens in the queue")

@@ -191,6 +191,22 @@ DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
 DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 8 * b; }
 
 // ================================================================== PREP
+// A token without a valid column on the queue path: o = 0, scale codes 0, LSE -inf,
+// written by the prep warp (the token never enters the pipeline).
+__device__ __noinline__ void write_empty_token(const KParams& P, int t, int lane) {
+  for (int i = lane; i < P.h_q * 32; i += 32) {
+    const int h = i >> 5, k = i & 31;
+    reinterpret_cast<uint4*>(P.out_fp8 + ((size_t)t * P.h_q + h) * D_LAT)[k] = make_uint4(0, 0, 0, 0);
+    if (P.out_precast) {
+      float4* pc = reinterpret_cast<float4*>(P.out_precast + ((size_t)t * P.h_q + h) * D_LAT);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pc[4 * k + u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  for (int i = lane; i < P.h_q * 16; i += 32) P.out_sf[(size_t)t * P.h_q * 16 + i] = 0;
+  if (P.out_lse)
+    for (int h = lane; h < P.h_q; h += 32) P.out_lse[(size_t)t * P.h_q + h] = -INFINITY;
+}
 // Items, row lists and rotary tables, one item ahead of the other roles.
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
@@ -220,15 +236,66 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     const int b = seq % NB;
     int* info = s_items + 8 * b;
     if (!wait_bar_w(c, B_ITEMPTY + b, ((seq / NB) & 1) ^ 1)) return;
-    const int item = __shfl_sync(0xFFFFFFFFu, next, 0);
-    if (item >= 0) next = fetch(seq + 1);
+    // Take items until one has tiles.  On the queue path a token without a valid column
+    // never enters the pipeline: its empty output is written here.  (The dequant warps
+    // hold an item until they have converted the first tile of the next item with
+    // tiles; a run of items without tiles could otherwise hold every buffer.)  The split
+    // path takes its one item as it is: the combine needs every split.
+    uint32_t* list = P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
+    int item, t = 0, split = 0, count = 0, T = 0, tile0 = 0, tile1 = 0;
+    while (true) {
+      item = __shfl_sync(0xFFFFFFFFu, next, 0);
+      if (item < 0) break;
+      next = fetch(seq + 1);
+      t = item / P.n_splits;
+      split = item % P.n_splits;
+      // compact the valid columns (j < topk_length, index >= 0), 512 indices per load batch
+      int L = P.topk_length[t];
+      L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
+      const int32_t* irow = P.indices + (size_t)t * P.topk;
+      count = 0;
+      for (int base = 0; base < L; base += 512) {
+        int v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int j = base + 32 * k + lane;
+          v[k] = (j < L) ? __ldg(irow + j) : -1;
+        }
+        // (not unrolled: the code of all roles shares the SM's instruction caches)
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k) {
+          const int j = base + 32 * k + lane;
+          const bool cmp = j >= P.n_swa_cols;
+          bool valid = v[k] >= 0;
+          if (valid && (P.flags & DSA_FLAG_CHECK_INDICES)) {
+            const long long nr = cmp ? P.n_cmp_rows : P.n_swa_rows;
+            if ((long long)v[k] >= nr) {
+              valid = false;
+              atomicOr(P.status, DSA_STATUS_INDEX_OUT_OF_RANGE);
+            }
+          }
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid);
+          if (valid) {
+            const uint32_t e = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
+            list[count + __popc(bal & ((1u << lane) - 1u))] = e;
+          }
+          count += __popc(bal);
+        }
+      }
+      const int n_tiles_tok = (count + TILE - 1) / TILE;
+      const int tps = (n_tiles_tok + P.n_splits - 1) / P.n_splits;
+      tile0 = split * tps;
+      tile1 = tile0 + tps;
+      if (tile1 > n_tiles_tok) tile1 = n_tiles_tok;
+      T = tile1 > tile0 ? tile1 - tile0 : 0;
+      if (split_path || T > 0) break;
+      write_empty_token(P, t, lane);
+    }
     if (item < 0) {
       if (lane == 0) info[IT_ITEM] = -1;
       mbar_arrive(bar(c, B_ITFULL + b));   // tells every role to stop
       return;
     }
-    const int t = item / P.n_splits;
-    const int split = item % P.n_splits;
     // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
     {
       float2* rope = reinterpret_cast<float2*>(c.sm + SM_ROPE) + 32 * b;
@@ -238,46 +305,6 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       sincospif(2.0f * frac, &sn, &cs);
       rope[lane] = make_float2(cs, sn);
     }
-    // compact the valid columns (j < topk_length, index >= 0), 512 indices per load batch
-    uint32_t* list = P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
-    int L = P.topk_length[t];
-    L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
-    const int32_t* irow = P.indices + (size_t)t * P.topk;
-    int count = 0;
-    for (int base = 0; base < L; base += 512) {
-      int v[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int j = base + 32 * k + lane;
-        v[k] = (j < L) ? __ldg(irow + j) : -1;
-      }
-      // (not unrolled: the code of all roles shares the SM's instruction caches)
-#pragma unroll 1
-      for (int k = 0; k < 16; ++k) {
-        const int j = base + 32 * k + lane;
-        const bool cmp = j >= P.n_swa_cols;
-        bool valid = v[k] >= 0;
-        if (valid && (P.flags & DSA_FLAG_CHECK_INDICES)) {
-          const long long nr = cmp ? P.n_cmp_rows : P.n_swa_rows;
-          if ((long long)v[k] >= nr) {
-            valid = false;
-            atomicOr(P.status, DSA_STATUS_INDEX_OUT_OF_RANGE);
-          }
-        }
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid);
-        if (valid) {
-          const uint32_t e = (uint32_t)v[k] | (cmp ? 0x80000000u : 0u);
-          list[count + __popc(bal & ((1u << lane) - 1u))] = e;
-        }
-        count += __popc(bal);
-      }
-    }
-    const int n_tiles_tok = (count + TILE - 1) / TILE;
-    const int tps = (n_tiles_tok + P.n_splits - 1) / P.n_splits;
-    const int tile0 = split * tps;
-    int tile1 = tile0 + tps;
-    if (tile1 > n_tiles_tok) tile1 = n_tiles_tok;
-    const int T = tile1 > tile0 ? tile1 - tile0 : 0;
     const int row0 = tile0 * TILE;
     const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
     __syncwarp();
@@ -1025,23 +1052,10 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
       for (int bi = 0; bi < nblk; ++bi)
         epi_chunk<16>(c, tmem, e, lane, is_split ? bi : 3 * bi, s_el, O, t, part, rope);
       ++nq;
-    } else {
-      // no valid column: o = 0, scale codes 0, LSE -inf
-      if (is_split) {
-        if (er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = -INFINITY;
-      } else {
-        for (int i = er; i < P.h_q * 32; i += N_EPI) {
-          const int h = i >> 5, k = i & 31;
-          reinterpret_cast<uint4*>(P.out_fp8 + ((size_t)t * P.h_q + h) * D_LAT)[k] = make_uint4(0, 0, 0, 0);
-          if (P.out_precast) {
-            float4* pc = reinterpret_cast<float4*>(P.out_precast + ((size_t)t * P.h_q + h) * D_LAT);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pc[4 * k + u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-        for (int i = er; i < P.h_q * 16; i += N_EPI) P.out_sf[(size_t)t * P.h_q * 16 + i] = 0;
-        if (P.out_lse && er < P.h_q) P.out_lse[(size_t)t * P.h_q + er] = -INFINITY;
-      }
+    } else if (is_split) {
+      // a split without a valid column: LSE -inf, so the combine gives it no weight
+      // (on the queue path such tokens never reach this role: the prep warp writes them)
+      if (er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = -INFINITY;
     }
     if (is_split) {
       // this split's partial is out: it counts in, and after the CTA's roles have
