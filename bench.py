@@ -56,11 +56,11 @@ def algorithmic_flops(w) -> int:
 
 def kernels_per_call(params) -> int:
     """Kernels one forward call launches: the fused kernel, preceded on the queue path
-    (no token split, at most 65536 tokens) by the kernel that orders the queue.  The split
-    path clears its workspace with a memset instead."""
+    (no token split, at most DSA_ORDER_MAX_TOKENS tokens) by the kernel that orders the
+    queue.  Otherwise a memset clears the workspace header instead."""
     from top_sparse_mla_gb300 import native
     queue = native.dsa_sparse_attn_num_splits(params, 0) == 1
-    return 2 if queue and params.s_q <= 65536 else 1
+    return 2 if queue and params.s_q <= native.DSA_ORDER_MAX_TOKENS else 1
 
 
 def profiled_traffic(workload_name: str):

@@ -37,7 +37,8 @@
  *               a token with no valid column (debug entry only; may be NULL)
  *
  * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream),
- * allocate nothing, and enqueue at most two kernels and one small memset (below).
+ * allocate nothing, and enqueue two operations: a small memset or a one-CTA ordering
+ * kernel, then the fused kernel (see dsa_sparse_attn_fwd).
  * Arguments are checked on the host before anything is enqueued; a non-zero
  * return means nothing was enqueued (DSA_ERR_CUDA: the launch itself failed).
  * An index >= its pool's row count is undefined behaviour unless
@@ -79,6 +80,7 @@ extern "C" {
 
 #define DSA_MAX_HEADS 64
 #define DSA_MAX_TOPK 2048
+#define DSA_ORDER_MAX_TOKENS 65536 /* above this the queue takes tokens in index order */
 #define DSA_ROW_BYTES 656
 #define DSA_NOALLOC_SCRATCH_BYTES (24u << 20) /* built-in scratch of the no-alloc entry */
 
@@ -116,10 +118,10 @@ size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
  *   splits of a token can wait for one another before each combines its share of the
  *   partial outputs; the grid is at most one CTA per SM.
  * - Otherwise the CTAs (at most one per SM) take tokens from one queue. With at most
- *   65536 tokens, a one-CTA kernel first clears the header and orders the queue: tokens
- *   with the most 128-row tiles (from topk_length) come first, equal counts in token
- *   order. The fused kernel is launched as its programmatic dependent. Above 65536
- *   tokens a memset clears the header and tokens go in index order.
+ *   DSA_ORDER_MAX_TOKENS tokens, a one-CTA kernel first clears the header and orders
+ *   the queue: tokens with the most 128-row tiles (from topk_length) come first, equal
+ *   counts in token order. The fused kernel is launched as its programmatic dependent.
+ *   With more tokens, a memset clears the header and tokens go in index order.
  * The order decides which CTA computes a token, never the token's result. */
 int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp,
                         const int32_t* indices, const int32_t* topk_length,

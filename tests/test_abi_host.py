@@ -47,6 +47,13 @@ def test_header_constants_match_the_binding():
         assert getattr(native, name) == value, name
 
 
+def test_order_bound_matches_the_kernel_source():
+    # the kernel keeps its own copy of the bound above which the queue is not ordered
+    src = open(os.path.join(ROOT, "top_sparse_mla_gb300", "csrc", "dsa_sparse_attn.cu")).read()
+    m = re.search(r"constexpr int ORDER_MAX_TOKENS = ([0-9]+);", src)
+    assert m and int(m.group(1)) == native.DSA_ORDER_MAX_TOKENS
+
+
 def test_flag_mask(lib):
     # both defined flags pass the argument check (num_splits returns 0 on a bad argument)
     p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096,

@@ -28,7 +28,7 @@ import parity
 pytestmark = pytest.mark.gpu
 
 HEADER_BYTES = 256
-ORDER_MAX_TOKENS = 65536
+ORDER_MAX_TOKENS = native.DSA_ORDER_MAX_TOKENS
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -26,6 +26,7 @@ DSA_STATUS_INDEX_OUT_OF_RANGE = 1
 DSA_STATUS_WAIT_TIMEOUT = 2
 DSA_MAX_HEADS = 64
 DSA_MAX_TOPK = 2048
+DSA_ORDER_MAX_TOKENS = 65536
 DSA_ROW_BYTES = 656
 DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 
