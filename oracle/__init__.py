@@ -17,9 +17,11 @@ Modules:
   codecs      -- e4m3 / bf16 / fp32 / UE8M0 encodings written from their definitions
   sparse_mla  -- the forward pass, one token at a time, in float64
   brute       -- a scalar pure-Python restatement for tiny inputs (cross-check)
+  topk        -- the index producer's top-k column selection (vLLM PR #64364, Claims
+                 and Validation), which has no CUDA path yet
 """
 
-from . import codecs, sparse_mla, brute  # noqa: F401
+from . import codecs, sparse_mla, brute, topk  # noqa: F401
 from .sparse_mla import (  # noqa: F401
     OracleParams,
     decode_kv_rows,
