@@ -18,7 +18,7 @@ Modules:
   sparse_mla  -- the forward pass, one token at a time, in float64
   brute       -- a scalar pure-Python restatement for tiny inputs (cross-check)
   topk        -- the index producer's top-k column selection (vLLM PR #64364, Claims
-                 and Validation), which has no CUDA path yet
+                 and Validation)
 """
 
 from . import codecs, sparse_mla, brute, topk  # noqa: F401

@@ -24,8 +24,8 @@ Readings where the page is silent (each also listed in the design notes):
   * The page's "remap" of the selected columns is not defined there and is not part
     of this function.
 
-Parity: this selection has no CUDA path yet; it is pinned against a brute-force
-enumeration and against torch.topk in the CPU tests.
+Parity: pinned against a brute-force enumeration and against torch.topk in the CPU
+tests. The CUDA path (dsa_topk_select) is compared with it bit for bit on the GPU.
 """
 
 from __future__ import annotations

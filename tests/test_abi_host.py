@@ -12,6 +12,7 @@ from top_sparse_mla_gb300.build import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "dsa_sparse_attn.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +22,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(dsa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
 
@@ -41,8 +42,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_header_constants_match_the_binding():
     # "#define NAME 2u", "#define NAME (-1)" and "#define NAME (24u << 20)"
     pattern = re.compile(r"^#define (DSA_[A-Z0-9_]+) \(?(-?[0-9]+)u?(?: << ([0-9]+))?", re.M)
-    defines = {name: int(v) << int(shift or 0) for name, v, shift in pattern.findall(open(HEADER).read())}
-    assert "DSA_FLAG_TEST_WAIT_TIMEOUT" in defines and "DSA_STATUS_WAIT_TIMEOUT" in defines
+    defines = {name: int(v) << int(shift or 0) for h in HEADERS for name, v, shift in pattern.findall(open(h).read())}
+    assert "DSA_FLAG_TEST_WAIT_TIMEOUT" in defines and "DSA_TOPK_MAX_COLS" in defines
     for name, value in defines.items():
         assert getattr(native, name) == value, name
 
@@ -62,6 +63,24 @@ def test_flag_mask(lib):
     for bad in (4, 8, 1 << 31):
         p.flags = bad
         assert native.dsa_sparse_attn_num_splits(p, 152) == 0
+
+
+def test_topk_select_checks_arguments_before_the_device(lib):
+    ok = native.DSA_OK
+    fake = 1 << 20   # a 16-byte aligned address that is never dereferenced on the host
+    f = lib.dsa_topk_select
+    bad = native.DSA_ERR_INVALID_ARG
+    assert f(fake, 100, None, -1, 100, 8, fake, fake, None) == bad          # s_q < 0
+    assert f(fake, 100, None, 4, 0, 8, fake, fake, None) == bad             # n < 1
+    assert f(fake, 70000, None, 4, native.DSA_TOPK_MAX_COLS + 1, 8, fake, fake, None) == bad
+    assert f(fake, 100, None, 4, 100, native.DSA_TOPK_MAX_K + 1, fake, fake, None) == bad
+    assert f(fake, 99, None, 4, 100, 8, fake, fake, None) == bad            # ld < n
+    assert f(None, 100, None, 4, 100, 8, fake, fake, None) == bad           # no logits
+    assert f(fake, 100, None, 4, 100, 8, None, fake, None) == bad           # no indices with k > 0
+    assert f(fake + 1, 100, None, 4, 100, 8, fake, fake, None) == bad       # misaligned logits
+    assert f(fake, 100, None, 0, 100, 8, None, None, None) == ok            # an empty batch is a no-op
+    # valid arguments reach the device check, which fails without a GPU
+    assert f(fake, 100, None, 4, 100, 8, fake, fake, None) in (native.DSA_ERR_CUDA, native.DSA_ERR_UNSUPPORTED_DEVICE)
 
 
 def test_params_init_defaults(lib):

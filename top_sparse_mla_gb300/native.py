@@ -27,6 +27,8 @@ DSA_STATUS_WAIT_TIMEOUT = 2
 DSA_MAX_HEADS = 64
 DSA_MAX_TOPK = 2048
 DSA_ORDER_MAX_TOKENS = 65536
+DSA_TOPK_MAX_COLS = 65536
+DSA_TOPK_MAX_K = 2048
 DSA_ROW_BYTES = 656
 DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 
@@ -39,6 +41,7 @@ EXPORTED = (
     "dsa_sparse_attn_read_status",
     "dsa_sparse_attn_num_splits",
     "dsa_error_string",
+    "dsa_topk_select",
 )
 
 
@@ -93,6 +96,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_sparse_attn_read_status.restype = ctypes.c_int
     lib.dsa_error_string.argtypes = [ctypes.c_int]
     lib.dsa_error_string.restype = ctypes.c_char_p
+    lib.dsa_topk_select.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp]
+    lib.dsa_topk_select.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -164,6 +169,20 @@ def dsa_sparse_attn_fwd_noalloc(q, kv_swa, kv_cmp, indices, topk_length, positio
                                                _ptr(out_sf), ctypes.byref(p), _ptr(status_out), _stream(stream))
     if rc != DSA_OK:
         raise DsaError(rc, "dsa_sparse_attn_fwd_noalloc")
+
+
+def dsa_topk_select(logits, k: int, indices, topk_length, lengths=None, stream=None) -> None:
+    """Top-k column selection (include/dsa_topk.h). logits: bf16 [s_q, ld] device tensor
+    whose first n = logits.shape[1] columns are the candidates; indices: int32 [s_q, k];
+    topk_length: int32 [s_q]; lengths: int32 [s_q] or None."""
+    s_q, n = int(logits.shape[0]), int(logits.shape[1])
+    if s_q > 0 and int(logits.stride(1)) != 1:
+        raise DsaError(DSA_ERR_INVALID_ARG, "dsa_topk_select: logits rows must be contiguous")
+    ld = int(logits.stride(0)) if s_q > 0 else n
+    rc = library().dsa_topk_select(_ptr(logits), ld, _ptr(lengths), s_q, n, int(k), _ptr(indices),
+                                   _ptr(topk_length), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_topk_select")
 
 
 def dsa_sparse_attn_read_status(workspace, stream=None) -> int:
