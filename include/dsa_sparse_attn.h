@@ -2,9 +2,9 @@
  * dsa_sparse_attn.h -- C ABI of the fused top-k sparse latent-attention kernel for
  * NVIDIA GB300 (sm_103a).
  *
- * Operation (stages as named on "Deepseek V41 Attention MegaKernel", vLLM PR #56344,
- * Purpose: fused norm + RoPE + sparse attention + inverse RoPE + FP8 cast).  For every
- * query token t and head h:
+ * Operation: the stages that the Purpose section of "Deepseek V41 Attention MegaKernel"
+ * (vLLM PR #56344) lists as fused, namely the query norm, RoPE, sparse attention,
+ * inverse RoPE and an FP8 cast of the output.  For every query token t and head h:
  *   1. q~ = RMSNorm(q[t,h,:576]) * norm_w   (fp32 statistics, eps = rms_eps)
  *   2. RoPE on q~ dims 512..575: pairs (512+2i, 513+2i) rotated by
  *      positions[t] * rope_base^(-2i/64)

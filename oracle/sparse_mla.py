@@ -1,8 +1,8 @@
 """Float64 definition of fused top-k sparse latent attention (oracle; test infrastructure only).
 
-What is computed, per query token t and head h (stages named on "Deepseek V41 Attention
-MegaKernel", vLLM PR #56344, Purpose: "fused norm + RoPE + sparse-attention +
-inverse-RoPE + FP8-cast"):
+What is computed, per query token t and head h.  The stages are the ones the Purpose
+section of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344) lists as fused: the
+query norm, RoPE, sparse attention, inverse RoPE and an FP8 cast of the output.
 
 1. q RMSNorm over all 576 dims of the head, times a shared 576-long weight.
 2. q RoPE on the last 64 dims (interleaved pairs, theta_i = base^(-2i/64), angle
