@@ -7,9 +7,12 @@
 // One CTA per row.  The row's bf16 logits become 16-bit keys in shared memory whose
 // unsigned order is the value order: every NaN maps to the largest key (torch.topk
 // ranks NaN above +inf), and -0 maps to +0's key (equal values, equal keys).  Two 8-bit
-// radix-select passes find the k-th largest key T and the number of keys above it.  An
-// ordered compaction over the columns then writes every column above T and the first
-// `need` columns equal to T, in ascending order.
+// radix-select passes find the k-th largest key T and the number of keys above it.  The
+// row is then cut into 32 contiguous segments, one per warp.  Each warp counts its keys
+// above T and equal to T (ballots, no block barrier).  One prefix over the warps gives
+// each warp the number of columns selected before its segment: those above T, plus the
+// equal ones up to `need`.  Each warp then writes its selected columns in order, so the
+// output is ascending and the first `need` columns equal to T are the lowest-numbered.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -27,42 +30,17 @@ __device__ __forceinline__ uint32_t order_key(uint32_t b) {
   return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-// Exclusive block-wide count of `v` over the threads in order; `total` gets the sum.
-// Every thread of the block calls it (it holds two barriers).
-__device__ __forceinline__ int block_excl_count(bool v, int* s_warp, int& total) {
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const unsigned bal = __ballot_sync(0xFFFFFFFFu, v);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) s_warp[w] = __popc(bal);
-  __syncthreads();
-  if (w == 0) {
-    const int x = s_warp[lane];   // WARPS == 32: one entry per lane
-    int incl = x;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-      if (lane >= d) incl += y;
-    }
-    s_warp[32 + lane] = incl - x;
-    if (lane == 31) s_warp[64] = incl;
-  }
-  __syncthreads();
-  total = s_warp[64];
-  const int r = s_warp[32 + w] + in_warp;
-  __syncthreads();   // s_warp is reused by the next call
-  return r;
-}
-
 __global__ void __launch_bounds__(THREADS, 1) topk_kernel(const uint16_t* __restrict__ logits, long long ld,
                                                           const int32_t* __restrict__ lengths, int n, int k,
                                                           int32_t* __restrict__ indices,
                                                           int32_t* __restrict__ topk_length) {
   extern __shared__ uint16_t s_key[];   // [n]
   __shared__ int s_hist[256];
-  __shared__ int s_warp[65];
+  __shared__ int s_gt[WARPS], s_eq[WARPS];
   __shared__ int s_sel[2];
-  static_assert(WARPS == 32, "one warp total per lane of warp 0");
-  const int tid = threadIdx.x;
+  static_assert(WARPS == 32, "one warp count per lane");
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const unsigned lt = (1u << lane) - 1u;
   const long long t = blockIdx.x;
   int L = n;
   if (lengths) {
@@ -121,20 +99,38 @@ __global__ void __launch_bounds__(THREADS, 1) topk_kernel(const uint16_t* __rest
   __syncthreads();
   const int T = (hi << 8) | s_sel[0];
   const int need = k - s_sel[1];   // columns equal to T to take, lowest first
-  // ordered compaction: columns above T, and the first `need` columns equal to T
-  int written = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < L; c0 += THREADS) {
-    const int j = c0 + tid;
-    const int key = j < L ? (int)s_key[j] : -1;
-    const bool eq = key == T;
-    int eq_total;
-    const int eq_rank = eq_seen + block_excl_count(eq, s_warp, eq_total);
-    const bool sel = key > T || (eq && eq_rank < need);
-    int sel_total;
-    const int pos = written + block_excl_count(sel, s_warp, sel_total);
+  // segment of warp w: columns [c_begin, c_end), a multiple of 32 long
+  const int seg = ((L + THREADS - 1) / THREADS) * 32;
+  const int c_begin = w * seg;
+  const int c_end = min(c_begin + seg, L);
+  int gt = 0, eq = 0;
+  for (int c = c_begin; c < c_end; c += 32) {
+    const int j = c + lane;
+    const int key = j < c_end ? (int)s_key[j] : -1;
+    gt += __popc(__ballot_sync(0xFFFFFFFFu, key > T));
+    eq += __popc(__ballot_sync(0xFFFFFFFFu, key == T));
+  }
+  if (lane == 0) {
+    s_gt[w] = gt;
+    s_eq[w] = eq;
+  }
+  __syncthreads();
+  // columns before this segment: above T, and equal to T
+  const int gt_before = __reduce_add_sync(0xFFFFFFFFu, lane < w ? s_gt[lane] : 0);
+  const int eq_before = __reduce_add_sync(0xFFFFFFFFu, lane < w ? s_eq[lane] : 0);
+  int eq_run = eq_before;
+  int sel_run = gt_before + min(eq_before, need);
+  for (int c = c_begin; c < c_end; c += 32) {
+    const int j = c + lane;
+    const int key = j < c_end ? (int)s_key[j] : -1;
+    const bool e = key == T;
+    const unsigned be = __ballot_sync(0xFFFFFFFFu, e);
+    const bool sel = key > T || (e && eq_run + __popc(be & lt) < need);
+    const unsigned bs = __ballot_sync(0xFFFFFFFFu, sel);
+    const int pos = sel_run + __popc(bs & lt);
     if (sel && pos < k) out[pos] = j;
-    written += sel_total;
-    eq_seen += eq_total;
+    eq_run += __popc(be);
+    sel_run += __popc(bs);
   }
   if (tid == 0) topk_length[t] = k;
 }
