@@ -54,12 +54,13 @@ def algorithmic_flops(w) -> int:
     return int(W.n_valid_rows(w).sum()) * (2 * w.h_q * 576 + 2 * w.h_q * 512)
 
 
-def kernels_per_call(params) -> int:
+def kernels_per_call(params, num_sms: int = 0) -> int:
     """Kernels one forward call launches: the fused kernel, preceded on the queue path
     (no token split, at most DSA_ORDER_MAX_TOKENS tokens) by the kernel that orders the
-    queue.  Otherwise a memset clears the workspace header instead."""
+    queue.  Otherwise a memset clears the workspace header instead.  num_sms <= 0: the
+    current device's SM count."""
     from top_sparse_mla_gb300 import native
-    queue = native.dsa_sparse_attn_num_splits(params, 0) == 1
+    queue = native.dsa_sparse_attn_num_splits(params, num_sms) == 1
     return 2 if queue and params.s_q <= native.DSA_ORDER_MAX_TOKENS else 1
 
 

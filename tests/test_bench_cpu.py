@@ -30,6 +30,20 @@ def test_reference_arm_prints_one_json_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
+def test_launch_count_per_call():
+    # queue path (no split, at most DSA_ORDER_MAX_TOKENS tokens): order kernel + fused
+    # kernel; split path and longer batches: a memset + the fused kernel
+    import bench
+    from top_sparse_mla_gb300 import native
+    native.library()
+    cases = [((1024, 64, 640, 128), 2), ((2123, 64, 640, 128), 2), ((1, 64, 640, 128), 1),
+             ((64, 64, 640, 128), 1), ((4, 64, 128, 64), 2),
+             ((native.DSA_ORDER_MAX_TOKENS + 1, 64, 640, 128), 1)]
+    for (s_q, h_q, topk, n_swa), want in cases:
+        p = native.dsa_params_init(s_q, h_q, topk, n_swa, 1 << 20, 1 << 20)
+        assert bench.kernels_per_call(p, 152) == want, (s_q, topk)
+
+
 def test_algorithmic_bytes_of_the_headline_workload():
     # the valid gathered rows (656 B each) plus, per token, q (64 heads x 576 bf16), the
     # codes and scales of the output, the index row, the length and the position
