@@ -31,7 +31,10 @@ E4M3_NAN_CODE = 0x7F
 
 
 def e4m3_decode(codes) -> np.ndarray:
-    """Decode E4M3 codes (uint8 array) to float64 values, NaN for S.1111.111."""
+    """Decode E4M3 codes (uint8 array) to float64 values, NaN for S.1111.111.
+
+    Format: OCP FP8 E4M3, the element format of the fp8_ds_mla cache and of the MXFP8 output.
+    """
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
     sign = (c >> 7) & 1
     exp_field = (c >> 3) & 0xF
@@ -54,6 +57,8 @@ def e4m3_encode(x) -> np.ndarray:
 
     NaN maps to the NaN code 0x7F.  The sign of zero is kept (0x80 for -0 and for
     negative values that round to zero).
+
+    Format: OCP FP8 E4M3 with round-to-nearest-even and saturation (a reading).
     """
     x = np.asarray(x, dtype=np.float64)
     neg = np.signbit(x)
@@ -84,6 +89,8 @@ def e4m3_ulp_distance(a_codes, b_codes) -> np.ndarray:
     """Distance between two E4M3 codes counted in steps of the E4M3 value lattice.
 
     Both codes must be finite.  Positive and negative zero are the same point.
+
+    Used by the FP8-code matching criterion of the tests, not by the path itself.
     """
     def ordinal(c):
         c = np.asarray(c, dtype=np.uint8).astype(np.int64)
@@ -93,19 +100,28 @@ def e4m3_ulp_distance(a_codes, b_codes) -> np.ndarray:
 
 
 def bf16_decode(bits) -> np.ndarray:
-    """bfloat16 bit patterns (uint16) to float64."""
+    """bfloat16 bit patterns (uint16) to float64.
+
+    Format: bfloat16, the type of q, the norm weight and the rope part of a cache row.
+    """
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     with np.errstate(invalid="ignore"):
         return b.view(np.float32).astype(np.float64)
 
 
 def fp32_decode_le(raw) -> np.ndarray:
-    """Little-endian IEEE binary32 from a uint8 array whose last axis is a multiple of 4."""
+    """Little-endian IEEE binary32 from a uint8 array whose last axis is a multiple of 4.
+
+    Format: IEEE binary32, the per-128 scales of an fp8_ds_mla row.
+    """
     r = np.ascontiguousarray(np.asarray(raw, dtype=np.uint8))
     return r.view("<f4").astype(np.float64)
 
 
 def ue8m0_decode(codes) -> np.ndarray:
+    """UE8M0 codes to their scale 2^(code - 127), NaN for code 255.
+
+    Format: OCP MX scale (a reading)."""
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
     v = np.ldexp(1.0, c - 127)
     return np.where(c == 255, np.nan, v)
@@ -113,7 +129,12 @@ def ue8m0_decode(codes) -> np.ndarray:
 
 def mx_shared_exponent(amax) -> np.ndarray:
     """Shared exponent of an MX block with E4M3 elements: floor(log2 amax) - 8,
-    clamped to the UE8M0 range [-127, 127]; a block of zeros takes -127 (code 0)."""
+    clamped to the UE8M0 range [-127, 127]; a block of zeros takes -127 (code 0).
+
+    Rule: OCP MX for E4M3 elements, the UE8M0 conversion that "[DSV4.1] Combine DSpark
+    decode and prefill kernel optimizations" (SGLang PR #39370), first description block
+    refers to (a reading).
+    """
     a = np.asarray(amax, dtype=np.float64)
     pos = a > 0
     e = np.where(pos, _floor_log2(np.where(pos, a, 1.0)) - E4M3_EMAX, -127)
@@ -126,6 +147,10 @@ def mxfp8_quantize(x, block: int = 32):
     The last axis must be a multiple of ``block``.  Each block's elements are divided
     by 2^E (E = ``mx_shared_exponent`` of the block's largest magnitude) and rounded
     to E4M3 with ties to even and saturation.
+
+    Rule: OCP MX block quantisation, the MXFP8 epilogue of "[DSV4.1] Combine DSpark decode
+    and prefill kernel optimizations" (SGLang PR #39370), first description block (a
+    reading).
     """
     x = np.asarray(x, dtype=np.float64)
     n = x.shape[-1]

@@ -7,7 +7,7 @@ query norm, RoPE, sparse attention, inverse RoPE and an FP8 cast of the output.
 1. q RMSNorm over all 576 dims of the head, times a shared 576-long weight.
 2. q RoPE on the last 64 dims (interleaved pairs, theta_i = base^(-2i/64), angle
    positions[t] * theta_i).  The pages give only the base (10000); the pair layout is
-   a reading, recorded with the other readings in the design notes.
+   a reading.
 3. Valid columns: j < topk_length[t] with indices[t, j] >= 0 (the page's sentinel fix:
    sparse reads are capped at topk_length and -1 entries are never read).  Columns
    [0, n_swa_cols) index the sliding-window cache, the rest the compressed cache
@@ -52,14 +52,22 @@ class OracleParams:
 
 
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
-    """x / sqrt(mean(x^2) + eps) * w along the last axis (float64)."""
+    """x / sqrt(mean(x^2) + eps) * w along the last axis (float64).
+
+    Step 1, the query norm of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344), Purpose;
+    its span (all 576 dims) and eps are a reading, the pages fix neither.
+    """
     x = np.asarray(x, dtype=np.float64)
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
 
 
 def rope_interleaved(x: np.ndarray, pos: float, base: float, inverse: bool = False) -> np.ndarray:
-    """Rotate consecutive pairs (2i, 2i+1) of the last axis by pos * base^(-2i/n)."""
+    """Rotate consecutive pairs (2i, 2i+1) of the last axis by pos * base^(-2i/n).
+
+    Steps 2 and 6, RoPE and inverse RoPE of "Deepseek V41 Attention MegaKernel" (vLLM PR
+    #56344), Purpose; the pair layout is a reading, the pages give only the base.
+    """
     x = np.asarray(x, dtype=np.float64)
     n = x.shape[-1]
     i = np.arange(n // 2, dtype=np.float64)
@@ -77,7 +85,10 @@ def rope_interleaved(x: np.ndarray, pos: float, base: float, inverse: bool = Fal
 
 
 def q_prologue(q_bits: np.ndarray, norm_w_bits: np.ndarray, pos: int, p: OracleParams) -> np.ndarray:
-    """Steps 1-2 for one token: bf16 q [h, 576] -> normalised, rotated q~ [h, 576]."""
+    """Steps 1-2 for one token: bf16 q [h, 576] -> normalised, rotated q~ [h, 576].
+
+    Steps 1-2 of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344), Purpose.
+    """
     x = codecs.bf16_decode(q_bits)
     w = codecs.bf16_decode(norm_w_bits)
     xn = rmsnorm(x, w, p.rms_eps)
@@ -86,7 +97,12 @@ def q_prologue(q_bits: np.ndarray, norm_w_bits: np.ndarray, pos: int, p: OracleP
 
 
 def decode_kv_rows(rows: np.ndarray) -> np.ndarray:
-    """fp8_ds_mla rows uint8 [n, 656] -> float64 k [n, 576] (v is k[:, :512])."""
+    """fp8_ds_mla rows uint8 [n, 656] -> float64 k [n, 576] (v is k[:, :512]).
+
+    Step 4: the fp8_ds_mla cache that "Deepseek V41 Attention MegaKernel" (vLLM PR #56344),
+    Purpose and its Performance section name; the byte layout is a reading, the pages give
+    none.
+    """
     rows = np.asarray(rows, dtype=np.uint8)
     assert rows.ndim == 2 and rows.shape[1] == ROW_BYTES
     n = rows.shape[0]
@@ -99,7 +115,11 @@ def decode_kv_rows(rows: np.ndarray) -> np.ndarray:
 
 
 def valid_columns(index_row: np.ndarray, topk_length: int) -> np.ndarray:
-    """Columns j < topk_length with a non-negative index (step 3)."""
+    """Columns j < topk_length with a non-negative index (step 3).
+
+    Step 3: the sentinel and topk_length rule of the bug-fix bullet of "Deepseek V41
+    Attention MegaKernel" (vLLM PR #56344), Purpose.
+    """
     topk = index_row.shape[0]
     n = max(0, min(int(topk_length), topk))
     cols = np.arange(n)
@@ -107,7 +127,12 @@ def valid_columns(index_row: np.ndarray, topk_length: int) -> np.ndarray:
 
 
 def gather_rows(index_row, cols, kv_swa, kv_cmp, n_swa_cols):
-    """Fetch the cache row of every valid column, choosing the cache by column."""
+    """Fetch the cache row of every valid column, choosing the cache by column.
+
+    Step 3: one combined index row per token (SWA columns first), as the
+    combine_topk_swa_indices bullet of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344),
+    Purpose describes.
+    """
     out = np.empty((len(cols), ROW_BYTES), dtype=np.uint8)
     for k, j in enumerate(cols):
         idx = int(index_row[j])
@@ -119,7 +144,13 @@ def gather_rows(index_row, cols, kv_swa, kv_cmp, n_swa_cols):
 
 
 def mxfp8_cast(o: np.ndarray):
-    """Step 7: (E4M3 codes, UE8M0 codes) along the last axis in 32-element blocks."""
+    """Step 7: (E4M3 codes, UE8M0 codes) along the last axis in 32-element blocks.
+
+    Step 7: the FP8 cast of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344), Purpose,
+    in the MXFP8 form of "[DSV4.1] Combine DSpark decode and prefill kernel optimizations"
+    (SGLang PR #39370), first description block (the UE8M0 rule is the OCP MX one, a
+    reading).
+    """
     return codecs.mxfp8_quantize(o, MX_BLOCK)
 
 
@@ -140,6 +171,8 @@ def sparse_mla_forward(q, kv_swa, kv_cmp, indices, topk_length, positions, norm_
       out_fp8      uint8 [s_q, h_q, 512]     E4M3 codes
       out_sf       uint8 [s_q, h_q, 16]      UE8M0 codes
       n_valid      int64 [s_q]
+
+    Steps 1-7 of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344), Purpose.
     """
     q = np.asarray(q)
     s_q, h_q, dq = q.shape

@@ -14,7 +14,7 @@ The same page says the attention reads each token's top-k directly, with no inde
 build in between.  This function's output therefore has the shape of the attention's
 ``indices`` / ``topk_length`` inputs.
 
-Readings where the page is silent (each also listed in the design notes):
+Readings where the page is silent:
   * A row may have fewer candidate columns than the logits' width. Columns at or past
     ``lengths[t]`` are not candidates, which covers causal and ragged rows. With fewer
     than k candidates, all of them are selected.
