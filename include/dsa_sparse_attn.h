@@ -79,6 +79,7 @@ extern "C" {
 #define DSA_STATUS_WAIT_TIMEOUT 2u       /* an on-chip pipeline wait gave up; output invalid */
 
 #define DSA_MAX_HEADS 64
+#define DSA_MAX_DEVICES 64 /* device ordinals >= this return DSA_ERR_UNSUPPORTED_DEVICE */
 #define DSA_MAX_TOPK 2048
 #define DSA_ORDER_MAX_TOKENS 65536 /* above this the queue takes tokens in index order */
 #define DSA_ROW_BYTES 656

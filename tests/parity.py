@@ -1,26 +1,19 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI, run the
 oracle on the same seeded inputs, compare.
 
-Tolerances (the workload specification's matching rule for this path):
+Tolerances: the workload specification's matching rule for this path, as written:
   * pre-cast output (after inverse RoPE): max |err| <= 2e-2 and relative L2 <= 1e-2;
   * UE8M0 scale codes bit-exact, except blocks whose oracle amax lies within 1e-6
-    relative of a power of two, or where a power of two lies between the oracle's and
-    the kernel's block amax (the exponent is floor(log2 amax): when the two amax values
-    straddle a power of two within the pre-cast tolerance the decision flips, and the
-    kernel's decision is then checked bit-exactly on its own output below);
-  * E4M3 codes within 1 step of the E4M3 lattice on >= 99.5 % of the elements of the
-    blocks whose scale code matched.  (The specification asks 99.9 %; with fp16 MMA
-    operands that is out of reach: an element far below its block maximum sits on a
-    fine part of the E4M3 lattice, and an absolute pre-cast error of a few 1e-4 moves
-    it by more than one step.  A CPU model of the kernel's roundings reproduces the
-    measured 99.71-99.85 % and shows that exact K and V with only q~ rounded to fp16
-    still give 99.87-99.90 %.  The bar is a miss rate of 0.5 % with a 4-sigma binomial
-    allowance, so that cases with only a few thousand codes do not fail on noise);
-  * LSE: |err| <= 2e-2 (same absolute bound as the output; -inf exactly where no
-    column is valid).
+    relative of a power of two;
+  * E4M3 codes within one step of the E4M3 lattice on at least 99.9 % of the elements
+    of the blocks whose scale code matched;
+  * LSE: |err| <= 2e-2 (the output's absolute bound; -inf exactly where no column is
+    valid).
 Where floating point decides an integer (the block exponent, the E4M3 code) the
 decision is also re-taken by the oracle's cast on the kernel's own fp32 pre-cast
 output, which must reproduce the kernel's codes bit for bit.
+Every comparison is recorded in RECORDS (label, measured errors and fractions); the
+test session prints them at its end, so a green run keeps the numbers.
 """
 
 from __future__ import annotations
@@ -36,7 +29,9 @@ from top_sparse_mla_gb300.workloads import Workload
 OUT_MAX_ABS = 2e-2
 OUT_REL_L2 = 1e-2
 LSE_ABS = 2e-2
-FP8_ULP_FRACTION = 0.995   # derived bar, see the module docstring
+FP8_ULP_FRACTION = 0.999   # E4M3 codes within one step, fraction of elements
+SF_BAND_REL = 1e-6          # scale codes may differ only within this of a power of two
+RECORDS: list = []
 
 
 def run_gpu(w: Workload, flags: int = 0, debug: bool = True, device="cuda:0"):
@@ -67,23 +62,14 @@ def run_oracle(w: Workload):
                                      oracle.OracleParams(n_swa_cols=w.n_swa_cols))
 
 
-def near_power_of_two(amax: np.ndarray, rel: float = 1e-6) -> np.ndarray:
+def near_power_of_two(amax: np.ndarray, rel: float = SF_BAND_REL) -> np.ndarray:
     a = np.where(amax > 0, amax, 1.0)
     k = np.round(np.log2(a))
     return (amax > 0) & (np.abs(a / np.exp2(k) - 1.0) <= rel)
 
 
-def straddles_power_of_two(a: np.ndarray, b: np.ndarray) -> np.ndarray:
-    """True where floor(log2 a) != floor(log2 b) for positive a, b (a power of two lies
-    in between)."""
-    pos = (a > 0) & (b > 0)
-    fa = np.floor(np.log2(np.where(pos, a, 1.0)))
-    fb = np.floor(np.log2(np.where(pos, b, 1.0)))
-    return pos & (fa != fb)
-
-
 def compare(gpu: dict, ref: dict, tokens=None, label: str = "") -> dict:
-    """Assert the matching rules; return the measured errors."""
+    """Assert the matching rules; return (and record) the measured errors."""
     g_out, g_lse = gpu["out"], gpu["lse"]
     g_fp8, g_sf = gpu["out_fp8"], gpu["out_sf"]
     if tokens is not None:
@@ -94,32 +80,36 @@ def compare(gpu: dict, ref: dict, tokens=None, label: str = "") -> dict:
     max_abs = float(err.max()) if err.size else 0.0
     denom = float(np.linalg.norm(r_out))
     rel_l2 = float(np.linalg.norm(g_out - r_out) / denom) if denom > 0 else float(np.linalg.norm(g_out))
-    assert max_abs <= OUT_MAX_ABS, f"{label}: pre-cast max abs error {max_abs:.3e}"
-    assert rel_l2 <= OUT_REL_L2, f"{label}: pre-cast relative L2 error {rel_l2:.3e}"
     # LSE
     inf_r, inf_g = np.isneginf(r_lse), np.isneginf(g_lse)
-    assert np.array_equal(inf_r, inf_g), f"{label}: -inf LSE pattern differs"
     lse_err = float(np.max(np.abs(g_lse[~inf_r] - r_lse[~inf_r]))) if (~inf_r).any() else 0.0
-    assert lse_err <= LSE_ABS, f"{label}: LSE error {lse_err:.3e}"
     # scales: bit-exact outside the power-of-two band
     amax = np.max(np.abs(r_out.reshape(r_out.shape[:-1] + (16, 32))), axis=-1)
-    g_amax = np.max(np.abs(g_out.reshape(g_out.shape[:-1] + (16, 32))), axis=-1)
-    band = near_power_of_two(amax) | straddles_power_of_two(amax, g_amax)
-    sf_bad = (g_sf != ref["out_sf"]) & ~band
-    assert not sf_bad.any(), f"{label}: {int(sf_bad.sum())} UE8M0 codes differ outside the power-of-two band"
+    band = near_power_of_two(amax)
+    sf_diff = g_sf != ref["out_sf"]
+    sf_bad = int((sf_diff & ~band).sum())
     # codes: within one E4M3 step on >= 99.9 % of the elements of blocks whose scale matched
-    same_blk = np.repeat((g_sf == ref["out_sf"])[..., None], 32, axis=-1).reshape(g_fp8.shape)
+    same_blk = np.repeat((~sf_diff)[..., None], 32, axis=-1).reshape(g_fp8.shape)
     ulp = codecs.e4m3_ulp_distance(g_fp8, ref["out_fp8"])
     n = int(same_blk.sum())
     misses = int((ulp[same_blk] > 1).sum())
     frac = 1.0 - misses / n if n else 1.0
-    p = 1.0 - FP8_ULP_FRACTION
-    allowed = p * n + 4.0 * np.sqrt(p * (1 - p) * n)
-    assert misses <= allowed, f"{label}: {misses} of {n} E4M3 codes more than 1 step away (allowed {allowed:.1f})"
+    exact = float((ulp[same_blk] == 0).mean()) if n else 1.0
+    rec = {"label": label, "max_abs": max_abs, "rel_l2": rel_l2, "lse_abs": lse_err, "fp8_within_1": frac,
+           "fp8_exact": exact, "fp8_misses": misses, "codes": n, "sf_mismatch_blocks": int(sf_diff.sum()),
+           "sf_band_blocks": int(band.sum()), "blocks": int(g_sf.size)}
+    RECORDS.append(rec)
+    summary = (f"{label}: fp8 within 1 step {frac:.6f} ({misses} of {n} misses), exact {exact:.6f}, "
+               f"scale mismatches {int(sf_diff.sum())} ({sf_bad} outside the 1e-6 band), "
+               f"max abs {max_abs:.3e}, rel L2 {rel_l2:.3e}, LSE {lse_err:.3e}")
+    assert max_abs <= OUT_MAX_ABS, f"pre-cast max abs error too large; {summary}"
+    assert rel_l2 <= OUT_REL_L2, f"pre-cast relative L2 error too large; {summary}"
+    assert np.array_equal(inf_r, inf_g), f"-inf LSE pattern differs; {summary}"
+    assert lse_err <= LSE_ABS, f"LSE error too large; {summary}"
+    assert sf_bad == 0, f"UE8M0 codes differ outside the power-of-two band; {summary}"
+    assert frac >= FP8_ULP_FRACTION, f"E4M3 codes more than one step away on too many elements; {summary}"
     # the kernel's own integer decisions, re-taken by the oracle cast on its fp32 output
     codes, sf = oracle.mxfp8_cast(g_out)
-    assert np.array_equal(sf, g_sf), f"{label}: scale codes differ from the oracle cast of the kernel's pre-cast output"
-    assert np.array_equal(codes, g_fp8), f"{label}: E4M3 codes differ from the oracle cast of the kernel's pre-cast output"
-    return {"max_abs": max_abs, "rel_l2": rel_l2, "lse_abs": lse_err, "fp8_within_1": frac,
-            "sf_exempt_blocks": int(band.sum()), "sf_mismatch_blocks": int((g_sf != ref["out_sf"]).sum()),
-            "blocks": int(g_sf.size)}
+    assert np.array_equal(sf, g_sf), f"scale codes differ from the oracle cast of the kernel's pre-cast output; {summary}"
+    assert np.array_equal(codes, g_fp8), f"E4M3 codes differ from the oracle cast of the kernel's output; {summary}"
+    return rec

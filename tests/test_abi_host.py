@@ -99,17 +99,36 @@ def test_error_strings(lib):
 def test_split_heuristic_and_workspace_size(lib):
     p = native.dsa_params_init(1, 64, 640, 128, 8192, 65536)
     assert native.dsa_sparse_attn_num_splits(p, 152) == 5          # one 128-row tile per split
+    # a work item is (token, half of the 64 heads): 64 tokens are 128 items on 152 SMs
     p = native.dsa_params_init(64, 64, 640, 128, 8192, 262144)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 1
+    p = native.dsa_params_init(64, 16, 640, 128, 8192, 262144)          # one half per token
     assert native.dsa_sparse_attn_num_splits(p, 152) == 2
     p = native.dsa_params_init(1024, 64, 640, 128, 131072, 1 << 20)
     assert native.dsa_sparse_attn_num_splits(p, 152) == 1
     ws1 = native.dsa_sparse_attn_workspace_size(p, 152)
     assert ws1 >= 256 + 4 * 1024 and ws1 % 256 == 0
-    p = native.dsa_params_init(64, 64, 640, 128, 8192, 262144)
+    p = native.dsa_params_init(32, 64, 640, 128, 8192, 262144)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 2
     ws2 = native.dsa_sparse_attn_workspace_size(p, 152)
-    assert ws2 >= 64 * 2 * 64 * 512 * 4                              # per-split partial outputs
+    assert ws2 >= 32 * 2 * 64 * 512 * 4                              # per-split partial outputs
     bad = native.dsa_params_init(1, 65, 640, 128, 1, 1)
     assert native.dsa_sparse_attn_workspace_size(bad, 152) == 0
+
+
+def test_every_split_path_shape_fits_the_no_alloc_scratch_on_152_sms(lib):
+    # The split path holds (s_q x splits) fp32 partial outputs; its item count, and so
+    # s_q x splits, is bounded by the SM count.  The largest such workspace on a 152-SM
+    # GB300 (76 tokens of at most 32 heads, 2048 columns, 2 splits) must fit the built-in
+    # scratch of the allocation-free entry point.
+    worst = 0
+    for h in (1, 16, 32, 33, 64):
+        for topk in (129, 640, 2048):
+            for s_q in range(1, 160):
+                p = native.dsa_params_init(s_q, h, topk, 0, 1, 1)
+                if native.dsa_sparse_attn_num_splits(p, 152) > 1:
+                    worst = max(worst, native.dsa_sparse_attn_workspace_size(p, 152))
+    assert 20 << 20 < worst <= native.DSA_NOALLOC_SCRATCH_BYTES
 
 
 def _call(lib, p, **over):

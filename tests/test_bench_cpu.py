@@ -37,7 +37,7 @@ def test_launch_count_per_call():
     from top_sparse_mla_gb300 import native
     native.library()
     cases = [((1024, 64, 640, 128), 2), ((2123, 64, 640, 128), 2), ((1, 64, 640, 128), 1),
-             ((64, 64, 640, 128), 1), ((4, 64, 128, 64), 2),
+             ((64, 64, 640, 128), 2), ((32, 64, 640, 128), 1), ((4, 64, 128, 64), 2),
              ((native.DSA_ORDER_MAX_TOKENS + 1, 64, 640, 128), 1)]
     for (s_q, h_q, topk, n_swa), want in cases:
         p = native.dsa_params_init(s_q, h_q, topk, n_swa, 1 << 20, 1 << 20)

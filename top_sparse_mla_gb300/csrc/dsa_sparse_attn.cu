@@ -3,32 +3,50 @@
 // MXFP8 cast, in one persistent kernel (stages as named on "Deepseek V41 Attention
 // MegaKernel", vLLM PR #56344, Purpose).
 //
-// Work item = (query token, KV split).  One CTA of 18 warps per SM; the warps are
-// specialised and talk through mbarriers:
+// Precision.  The two contractions run on fp16 tcgen05 MMAs with fp32 accumulation, and
+// every operand is either exact in fp16 or carried as an exact-enough hi + lo pair:
+//   - the latent tile holds the raw E4M3 codes (exact in fp16); each row's four fp32
+//     block scales are applied in fp32, per 128-dim block, outside the MMA: QK^T runs one
+//     partial score per block and the softmax warps add the partials times the scales;
+//     PV runs one block of output dims per scale block with P scaled by that block's
+//     scales (P_b = P * s_b);
+//   - q~ = q * w (exact in fp32: 8-bit by 8-bit significands) and P_b go in as hi + lo,
+//     both fp16; the MMA's N = 64 holds the work item's 32 heads twice, hi then lo, and
+//     the two accumulators are added in fp32.
+// A work item is therefore (query token, half of the heads, KV split): 32 heads.
+//
+// One CTA of 18 warps per SM; the warps are specialised and talk through mbarriers:
 //
 //   DQ   (warps 0-7)   when an item opens (right after the previous item's last QK^T):
-//                      q~ = RoPE(q * w) in fp16 as the B operand of QK^T, chunk by chunk,
-//                      and the fp32 RMS statistics of q.  Per tile: gathered rows -> fp16
-//                      latent tile [128 rows x 512 dims] in shared memory, fp32 block scale
-//                      folded in.  The one tile is the A operand of both contractions:
+//                      q~ hi/lo of its 32 heads as the B operand of QK^T, with a per-head
+//                      power-of-two prescale, and the fp32 RMS statistics of q.  Per tile:
+//                      gathered rows -> fp16 codes tile [128 rows x 512 dims] in shared
+//                      memory.  The one tile is the A operand of both contractions:
 //                      K-major for QK^T (M = rows), MN-major for PV (M = dims).  Raw bytes
 //                      are loaded two chunks ahead, rows are prefetched into L2 one tile
 //                      ahead.  Between items (no splits): the MXFP8 finish of output dims
 //                      128..383 of the previous item.
-//   SM   (warps 8-11)  per tile the softmax over S^T (lazy running max, exp2, fp16 P) with
-//                      the per-head factor softmax_scale * log2(e) / rms(q), and the rotary
-//                      part of the next tile's keys (bf16 -> fp16) into TMEM
-//   EPI  (warps 12-15) 1/l and the LSE; the epilogue: O^T / l out of TMEM into the global
-//                      output (dims 0..127 and 384..511, or all of it as a split partial)
-//   MMA  (warp 16)     S^T[128 rows x 64 heads] = K~ . q~^T; O^T[512 x 64] += V~^T . P;
-//                      l[64] += 1^T . P (row sums on the tensor core)
+//   SM   (warps 8-11)  per tile: the five partial scores (four latent blocks, rope) summed
+//                      with the row's block scales, the softmax (lazy running max, exp2),
+//                      per-warp row sums, P_b hi/lo for the four PV blocks; then the
+//                      rotary part and the block scales of the next tile's rows
+//   EPI  (warps 12-15) 1/l and the LSE; the epilogue: (O_hi + O_lo) / l out of TMEM into
+//                      the global output (dims 0..127 and 384..511, or all of it as a
+//                      split partial)
+//   MMA  (warp 16)     T_b[128 rows x 64] = codes_b . q~_b^T for b = 0..3 and the rope
+//                      part; O^T_b[128 dims x 64] += codes_b^T . P_b
 //   PREP (warp 17)     take an item, compact its valid index columns into a row list,
-//                      rotary table; up to three items ahead
+//                      the per-block reference scale of its rows, rotary table; up to
+//                      three items ahead
 //
-// TMEM: O^T 0..255, l 256..319, S^T 320..447 (two buffers), K~ rope part 448..511 (two).
+// TMEM: O^T 0..255 (4 blocks x [32 hi | 32 lo]), partial scores 256..447 (three
+// buffers), rope keys 448..511 (two).  Shared memory: q~ 72 KB, codes tile 128 KB, one
+// 16 KB P buffer.  P_1 and P_3 borrow the first halves of code chunks 0 and 1 once PV
+// of blocks 0 and 1 has read them, so the next tile's QK^T takes its chunks in the
+// order 0, 2, 1, 3, the order in which they come free.
 // With few tokens each token's rows are split over several CTAs, one item per CTA, and
-// the launch is cooperative: once its roles are done, every split of a token waits for
-// the others and combines its share of the fp32 partial outputs.
+// the launch is cooperative: once its roles are done, every split of a (token, half)
+// waits for the others and combines its share of the fp32 partial outputs.
 // Every wait is bounded; on timeout the CTA raises DSA_STATUS_WAIT_TIMEOUT, every role
 // leaves its loop, the tensor core is drained and TMEM freed.
 
@@ -47,55 +65,65 @@ constexpr int D_LAT = 512;
 constexpr int D_QK = 576;
 constexpr int ROW_BYTES = 656;
 constexpr int TILE = 128;           // gathered rows per tile (the M of QK^T)
-constexpr int HP = 64;              // heads as seen by the MMAs (padded)
+constexpr int HH = 32;              // heads per work item
+constexpr int NQ = 64;              // N of both contractions: 32 heads hi, then 32 lo
 constexpr int W_SM = 8, W_EPI = 12, W_MMA = 16, W_PREP = 17;
 constexpr int NWARPS = 18;
 constexpr int NTHREADS = 32 * NWARPS;
 constexpr int N_DQ = 256, N_SM = 128, N_EPI = 128, N_PREP = 32;
 constexpr int MAX_SPLITS = 16;
 constexpr int NB = 4;              // item buffers: the prep warp runs up to NB - 1 items ahead
+constexpr int NSB = 3;             // partial-score buffers in TMEM
+constexpr int NPART = 5;           // partial scores per tile: four latent blocks and the rope part
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
-constexpr uint32_t TM_L = 256;
-constexpr uint32_t TM_S = 320;      // + 64 * buffer
+constexpr uint32_t TM_S = 256;      // + 64 * buffer
 constexpr uint32_t TM_KR = 448;     // + 32 * buffer
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t SM_Q = 0;                       // q~: 9 K-atoms x [64 heads x 128 B]
-constexpr uint32_t SM_V = SM_Q + 9 * 8192;         // latent tile: 4 chunks x 2 halves x 16 KB
-constexpr uint32_t SM_P = SM_V + 4 * 32768;        // P: [128 rows x 64 heads] fp16
-constexpr uint32_t SM_ONES = SM_P + 16384;         // [128 x 16] fp16 ones (A of the row sums)
-constexpr uint32_t SM_ROPE = SM_ONES + 4096;       // NB x 32 x (cos, sin)
-constexpr uint32_t SM_INV = SM_ROPE + NB * 256;    // NB x 64 fp32: softmax_scale * log2(e) / rms(q)
-constexpr uint32_t SM_ITEM = SM_INV + NB * 256;    // NB x 8 ints
-constexpr uint32_t SM_M = SM_ITEM + NB * 32;       // 64 fp32 running max (log2 units)
-constexpr uint32_t SM_ALPHA = SM_M + 256;          // 64 fp32 rescale factors
-constexpr uint32_t SM_MFIN = SM_ALPHA + 256;       // 2 x 64 fp32 final max per item
-constexpr uint32_t SM_RED = SM_MFIN + 512;         // 4 warps x 64 fp32
-constexpr uint32_t SM_ESCL = SM_RED + 1024;        // 4 EPI warps x 32 fp32 block scales
-constexpr uint32_t SM_EL = SM_ESCL + 512;          // 64 fp32 row sums, then 1/l
-constexpr uint32_t SM_ELSE = SM_EL + 256;          // 64 fp32 LSE (log2 units)
-constexpr uint32_t SM_FLAG = SM_ELSE + 256;        // 2 x 4 fp32
+constexpr uint32_t SM_Q = 0;                       // q~: 9 K-atoms x [64 rows x 128 B]
+constexpr uint32_t SM_V = SM_Q + 9 * 8192;         // codes tile: 4 chunks x 2 halves x 16 KB
+constexpr uint32_t SM_P = SM_V + 4 * 32768;        // P_0 / P_2: [128 rows x 64] fp16
+constexpr uint32_t SM_ROPE = SM_P + 16384;         // NB x 32 x (cos, sin)
+constexpr uint32_t SM_INV = SM_ROPE + NB * 256;    // NB x 32 fp32 score factors
+constexpr uint32_t SM_ITEM = SM_INV + NB * 128;    // NB x 16 ints
+constexpr uint32_t SM_M = SM_ITEM + NB * 64;       // 32 fp32 running max (log2 units)
+constexpr uint32_t SM_ALPHA = SM_M + 128;          // 32 fp32 rescale factors
+constexpr uint32_t SM_MFIN = SM_ALPHA + 128;       // 2 x 32 fp32 final max per item
+constexpr uint32_t SM_RED = SM_MFIN + 256;         // 4 warps x 32 fp32
+constexpr uint32_t SM_LW = SM_RED + 512;           // 2 x 4 warps x 32 fp32 row-sum partials
+constexpr uint32_t SM_EL = SM_LW + 1024;           // 32 fp32 1/l
+constexpr uint32_t SM_ELSE = SM_EL + 128;          // 32 fp32 LSE (log2 units)
+constexpr uint32_t SM_FLAG = SM_ELSE + 128;        // 2 x 4 fp32
 constexpr uint32_t SM_MISC = SM_FLAG + 32;         // misc ints
 constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
-constexpr uint32_t SM_END = SM_BAR + 48 * 8;
+constexpr uint32_t SM_END = SM_BAR + 64 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-// after the last item the latent tile area holds the split-combine weights
+// after the last item the codes tile area holds the split-combine weights
 constexpr uint32_t SM_CW = SM_V;
 
 enum {
-  B_VFULL = 0, B_VFREE = B_VFULL + 4, B_KRFULL = B_VFREE + 4, B_KRFREE = B_KRFULL + 2,
-  B_SFULL = B_KRFREE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE,
-  B_ITFULL, B_ITEMPTY = B_ITFULL + NB, B_ODONE = B_ITEMPTY + NB, B_OFREE,
-  B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB, B_LREADY, B_SMG, B_EPG, B_DRAIN, B_NEVER, B_COUNT
+  B_VFULL = 0, B_PVD = B_VFULL + 4, B_PFULL = B_PVD + 4, B_SFULL = B_PFULL + 4, B_SFREE = B_SFULL + NSB,
+  B_KRFULL = B_SFREE + NSB, B_KRFREE = B_KRFULL + 2, B_ITFULL = B_KRFREE + 2, B_ITEMPTY = B_ITFULL + NB,
+  B_ODONE = B_ITEMPTY + NB, B_OFREE, B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB,
+  B_LREADY, B_SMG, B_EPG, B_DRAIN, B_NEVER, B_COUNT
 };
-static_assert(B_COUNT <= 48, "barrier area");
+static_assert(B_COUNT <= 64, "barrier area");
 
-enum { M_TMEM = 0, M_ABORT, M_COMBINE, M_TOKEN, M_SPLIT };         // misc ints
-enum { IT_ITEM = 0, IT_TOKEN, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS }; // item info ints
+enum { M_TMEM = 0, M_ABORT, M_COMBINE, M_TOKEN, M_SPLIT, M_HALF };   // misc ints
+// item info ints (16 per item buffer); IT_REF / IT_IREF hold 4 floats each
+enum { IT_ITEM = 0, IT_TOKEN, IT_HALF, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS, IT_REF = 8, IT_IREF = 12 };
+
+// The QK^T order of the latent chunks (p-th partial -> chunk), the PV event after which
+// chunk c of the codes tile may be overwritten by the next tile, and where P_b lives.
+DSA_DEV int qk_chunk(int p) { return p == 1 ? 2 : (p == 2 ? 1 : p); }
+DSA_DEV int chunk_free_event(int c) { return c == 0 ? 1 : (c == 2 ? 2 : 3); }
+DSA_DEV uint32_t p_buffer(int b) {
+  return b == 1 ? SM_V : (b == 3 ? SM_V + 32768u : SM_P);
+}
 
 struct KParams {
   const uint16_t* q;
@@ -111,7 +139,7 @@ struct KParams {
   float* out_lse;
   float* part_o;        // split partials [s_q][n_splits][64 heads][512 dims]
   float* part_lse;      // [s_q][n_splits][64] (log2 units)
-  uint32_t* counters;   // [s_q] split arrivals (split path)
+  uint32_t* counters;   // [s_q][n_halves] split arrivals (split path)
   const int32_t* order; // [s_q] tokens, most tiles first (queue path; shares the counters'
                         // region), or null: tokens in order
   uint32_t* status;
@@ -123,6 +151,7 @@ struct KParams {
   float rms_eps;
   uint32_t flags;
   int n_splits;
+  int n_halves;             // 1 when h_q <= 32, else 2
   int n_items;
   // rotary frequency of pair i as a 64-bit fixed-point fraction of a turn:
   // rope_base^(-2i/64) / (2 pi) * 2^64
@@ -188,14 +217,22 @@ DSA_DEV const uint8_t* row_ptr(const KParams& P, uint32_t e) {
 DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
   return P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
 }
-DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 8 * b; }
+DSA_DEV const int* item_info(const Ctx& c, int b) { return reinterpret_cast<const int*>(c.sm + SM_ITEM) + 16 * b; }
+DSA_DEV const float* item_ref(const Ctx& c, int b) {
+  return reinterpret_cast<const float*>(c.sm + SM_ITEM) + 16 * b + IT_REF;
+}
+DSA_DEV const float* item_iref(const Ctx& c, int b) {
+  return reinterpret_cast<const float*>(c.sm + SM_ITEM) + 16 * b + IT_IREF;
+}
 
 // ================================================================== PREP
-// A token without a valid column on the queue path: o = 0, scale codes 0, LSE -inf,
-// written by the prep warp (the token never enters the pipeline).
-__device__ __noinline__ void write_empty_token(const KParams& P, int t, int lane) {
-  for (int i = lane; i < P.h_q * 32; i += 32) {
-    const int h = i >> 5, k = i & 31;
+// A (token, half) without a valid column on the queue path: o = 0, scale codes 0, LSE
+// -inf, written by the prep warp (the item never enters the pipeline).
+__device__ __noinline__ void write_empty_item(const KParams& P, int t, int half, int lane) {
+  const int h0 = HH * half;
+  const int nh = (P.h_q - h0) < HH ? (P.h_q - h0) : HH;
+  for (int i = lane; i < nh * 32; i += 32) {
+    const int h = h0 + (i >> 5), k = i & 31;
     reinterpret_cast<uint4*>(P.out_fp8 + ((size_t)t * P.h_q + h) * D_LAT)[k] = make_uint4(0, 0, 0, 0);
     if (P.out_precast) {
       float4* pc = reinterpret_cast<float4*>(P.out_precast + ((size_t)t * P.h_q + h) * D_LAT);
@@ -203,26 +240,32 @@ __device__ __noinline__ void write_empty_token(const KParams& P, int t, int lane
       for (int u = 0; u < 4; ++u) pc[4 * k + u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  for (int i = lane; i < P.h_q * 16; i += 32) P.out_sf[(size_t)t * P.h_q * 16 + i] = 0;
-  if (P.out_lse)
-    for (int h = lane; h < P.h_q; h += 32) P.out_lse[(size_t)t * P.h_q + h] = -INFINITY;
+  for (int i = lane; i < nh * 16; i += 32) P.out_sf[((size_t)t * P.h_q + h0) * 16 + i] = 0;
+  if (P.out_lse && lane < nh) P.out_lse[(size_t)t * P.h_q + h0 + lane] = -INFINITY;
 }
-// Items, row lists and rotary tables, one item ahead of the other roles.
+
+DSA_DEV uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Items, row lists, reference scales and rotary tables, ahead of the other roles.
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
   const bool split_path = P.n_splits > 1;
   // split path: exactly one item per CTA (the grid has one CTA per item), so the last
-  // split of a token can run its combine with the whole CTA afterwards.  Otherwise items
-  // come from the global queue in the order of P.order (tokens with the most tiles
-  // first, so that the last items handed out are short ones), each fetched one iteration
-  // before it is used.
+  // split of a (token, half) can run its combine with the whole CTA afterwards.
+  // Otherwise items come from the global queue: position k is half k % n_halves of the
+  // token P.order[k / n_halves] (tokens with the most tiles first, so that the last items
+  // handed out are short ones; the halves of a token are adjacent, so the second reads
+  // the rows from L2), each fetched one iteration before it is used.
   auto fetch = [&](uint32_t seq) -> int {
     int item = 0;
     if (lane == 0) {
       if (split_path) item = seq == 0 ? (int)blockIdx.x : P.n_items;
       else item = (int)atomicAdd(P.work, 1u);
       item = item < P.n_items ? item : -1;
-      if (!split_path && item >= 0 && P.order) item = P.order[item];
     }
     return item;
   };
@@ -234,21 +277,29 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int next = fetch(0);
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq % NB;
-    int* info = s_items + 8 * b;
+    int* info = s_items + 16 * b;
     if (!wait_bar_w(c, B_ITEMPTY + b, ((seq / NB) & 1) ^ 1)) return;
-    // Take items until one has tiles.  On the queue path a token without a valid column
+    // Take items until one has tiles.  On the queue path an item without a valid column
     // never enters the pipeline: its empty output is written here.  (The dequant warps
     // hold an item until they have converted the first tile of the next item with
     // tiles; a run of items without tiles could otherwise hold every buffer.)  The split
     // path takes its one item as it is: the combine needs every split.
     uint32_t* list = P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
-    int item, t = 0, split = 0, count = 0, T = 0, tile0 = 0, tile1 = 0;
+    int item, t = 0, half = 0, split = 0, count = 0, T = 0, tile0 = 0, tile1 = 0;
     while (true) {
       item = __shfl_sync(0xFFFFFFFFu, next, 0);
       if (item < 0) break;
       next = fetch(seq + 1);
-      t = item / P.n_splits;
-      split = item % P.n_splits;
+      if (split_path) {
+        split = item % P.n_splits;
+        half = (item / P.n_splits) % P.n_halves;
+        t = item / (P.n_splits * P.n_halves);
+      } else {
+        const int k = item / P.n_halves;
+        half = item % P.n_halves;
+        t = P.order ? __ldcg(P.order + k) : k;
+        split = 0;
+      }
       // compact the valid columns (j < topk_length, index >= 0), 512 indices per load batch
       int L = P.topk_length[t];
       L = L < 0 ? 0 : (L > P.topk ? P.topk : L);
@@ -289,12 +340,32 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       if (tile1 > n_tiles_tok) tile1 = n_tiles_tok;
       T = tile1 > tile0 ? tile1 - tile0 : 0;
       if (split_path || T > 0) break;
-      write_empty_token(P, t, lane);
+      write_empty_item(P, t, half, lane);
     }
     if (item < 0) {
       if (lane == 0) info[IT_ITEM] = -1;
       mbar_arrive(bar(c, B_ITFULL + b));   // tells every role to stop
       return;
+    }
+    const int row0 = tile0 * TILE;
+    const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
+    __syncwarp();   // the list entries of the other lanes
+    // Reference scale of each latent block: the power of two at or below the largest
+    // |scale| of the item's rows, so that P_b = P * scale / reference stays below 2 P.
+    float mx[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = lane; i < nrows; i += 32) {
+      const uint4 s = ldg_nc(row_ptr(P, __ldcg(list + row0 + i)) + D_LAT);
+      mx[0] = fmaxf(mx[0], fabsf(__uint_as_float(s.x)));
+      mx[1] = fmaxf(mx[1], fabsf(__uint_as_float(s.y)));
+      mx[2] = fmaxf(mx[2], fabsf(__uint_as_float(s.z)));
+      mx[3] = fmaxf(mx[3], fabsf(__uint_as_float(s.w)));
+    }
+    uint32_t ebits[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int e = (int)((redux_max_u32(__float_as_uint(mx[k])) >> 23) & 0xFF);
+      e = e < 1 ? 1 : (e > 253 ? 253 : e);
+      ebits[k] = (uint32_t)e;
     }
     // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
     {
@@ -305,18 +376,20 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       sincospif(2.0f * frac, &sn, &cs);
       rope[lane] = make_float2(cs, sn);
     }
-    const int row0 = tile0 * TILE;
-    const int nrows = T > 0 ? ((tile1 * TILE < count ? tile1 * TILE : count) - row0) : 0;
-    __syncwarp();
     if (lane == 0) {
       info[IT_ITEM] = item;
       info[IT_TOKEN] = t;
+      info[IT_HALF] = half;
       info[IT_SPLIT] = split;
       info[IT_T] = T;
       info[IT_ROW0] = row0;
       info[IT_NROWS] = nrows;
     }
-    mbar_arrive(bar(c, B_ITFULL + b));   // rows, tile range, rotary table
+    if (lane < 4) {
+      info[IT_REF + lane] = (int)(ebits[lane] << 23);            // 2^(e - 127)
+      info[IT_IREF + lane] = (int)((254u - ebits[lane]) << 23);  // 2^(127 - e)
+    }
+    mbar_arrive(bar(c, B_ITFULL + b));   // rows, tile range, reference scales, rotary table
   }
 }
 
@@ -409,21 +482,23 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[N], int t, int h0, int 
 }
 
 // Epilogue of the 128-dim column block cidx of O^T by a warp on TMEM lane quarter q4
-// (dims 128 cidx + 32 q4 + lane), NH heads at a time, scaled by 1/l from s_il.  The
-// block is released on OFREE[cidx] once it and s_il have been read.  With part set the
-// normalised partial is stored instead of finished.
+// (dims 128 cidx + 32 q4 + lane), NH heads at a time: (O_hi + O_lo) times the block's
+// reference scale and 1/l from s_il.  The block is released on OFREE[cidx] once it has
+// been read.  With part set the normalised partial is stored instead of finished.
 template <int NH>
-DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, const float* s_il, const OutPtrs& O,
-                       int t, float* part, const float2* rope) {
+DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, const float* s_il, float ref,
+                       const OutPtrs& O, int t, int h0, float* part, const float2* rope) {
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
   const int d = 128 * cidx + 32 * q4 + lane;
 #pragma unroll 1
-  for (int hg = 0; hg < 64 / NH; ++hg) {
-    uint32_t a[NH];
+  for (int hg = 0; hg < HH / NH; ++hg) {
+    uint32_t a[NH], l[NH];
     if constexpr (NH == 16) {
       tmem_ld16(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
+      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + HH + NH * hg, l);
     } else {
       tmem_ld8(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
+      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + HH + NH * hg, l);
     }
     tc_wait_ld();
     const float4* il4 = reinterpret_cast<const float4*>(s_il + NH * hg);
@@ -431,12 +506,12 @@ DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, 
 #pragma unroll
     for (int q = 0; q < NH / 4; ++q) {
       const float4 f = il4[q];
-      v[4 * q] = __uint_as_float(a[4 * q]) * f.x;
-      v[4 * q + 1] = __uint_as_float(a[4 * q + 1]) * f.y;
-      v[4 * q + 2] = __uint_as_float(a[4 * q + 2]) * f.z;
-      v[4 * q + 3] = __uint_as_float(a[4 * q + 3]) * f.w;
+      v[4 * q] = (__uint_as_float(a[4 * q]) + __uint_as_float(l[4 * q])) * (ref * f.x);
+      v[4 * q + 1] = (__uint_as_float(a[4 * q + 1]) + __uint_as_float(l[4 * q + 1])) * (ref * f.y);
+      v[4 * q + 2] = (__uint_as_float(a[4 * q + 2]) + __uint_as_float(l[4 * q + 2])) * (ref * f.z);
+      v[4 * q + 3] = (__uint_as_float(a[4 * q + 3]) + __uint_as_float(l[4 * q + 3])) * (ref * f.w);
     }
-    if (hg == 64 / NH - 1) {
+    if (hg == HH / NH - 1) {
       tc_fence_before();
       mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
     }
@@ -445,21 +520,25 @@ DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, 
 #pragma unroll
       for (int i = 0; i < NH; ++i) o[(size_t)i * D_LAT] = v[i];
     } else {
-      finalize_lanes<NH>(O, v, t, NH * hg, d, lane, rope);
+      finalize_lanes<NH>(O, v, t, h0 + NH * hg, d, lane, rope);
     }
   }
 }
 
 // ================================================================== q~
-// q~ of one item without its RMS factor: q * w, RoPE on dims 512..575, fp16, as the B
-// operand of QK^T, built by the 256 dequant threads.  The per-head factor
-// softmax_scale * log2(e) / rms(q) multiplies the scores instead (the rotation and QK^T
-// are linear in q~), so the statistics need not come first.  64 heads x 9 atoms x 8
-// chunks of 8 dims: thread-piece j covers head (er / 8) + 32 (j % 2), chunk er % 8, atom
-// j / 2, so one warp reads four 128-byte head rows and writes them with conflict-free
-// swizzled stores.  Chunk c of the latent dims (atoms 2c, 2c + 1) is announced on
-// QRDY[c], the rotary atom on QRDY[4], so that QK^T can start before the whole of q~ is
-// written; the statistics follow on QSTAT[b].
+// q~ of one item without its RMS factor: q * w times a per-head power of two 2^k, RoPE
+// on dims 512..575, as an fp16 hi + lo pair, the B operand of QK^T: row n < 32 holds the
+// hi part of the item's head n, row 32 + n its lo part.  q * w is exact in fp32 (two
+// 8-bit significands) and has at most 16 significant bits, so hi + lo is exact on the
+// latent dims; on the rotated dims it is exact to about 2^-22.  2^k brings the head's
+// largest |q * w| into [2^13, 2^14): the rotated pairs stay inside the fp16 range and the
+// lo parts stay normal for every value that matters.  The per-head factor
+// softmax_scale * log2(e) / (rms(q) 2^k) multiplies the scores instead (the rotation and
+// QK^T are linear in q~).  Built by the 256 dequant threads in two passes over q (the
+// statistics and the largest magnitude, then the operand): thread er covers head er / 8
+// and the 8-dim chunk er % 8 of each of the 9 atoms.  Chunk c of the latent dims (atoms
+// 2c, 2c + 1) is announced on QRDY[c], the rotary atom on QRDY[4], so that QK^T can start
+// before the whole of q~ is written; the statistics follow on QSTAT[b].
 struct QArgs {
   const uint16_t* q;
   const uint16_t* norm_w;
@@ -468,98 +547,101 @@ struct QArgs {
 };
 
 DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
-  const uint16_t* qt = P.q + (size_t)item_info(c, b)[IT_TOKEN] * P.h_q * D_QK;
-  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  const int* info = item_info(c, b);
   const int hs = er >> 3, chn = er & 7;
-  float ss[2] = {0.f, 0.f};
-  // rounds of three atoms: six q pieces (two heads x three atoms) and three norm-weight
-  // pieces in flight per thread
-#pragma unroll 1
-  for (int a0 = 0; a0 < 9; a0 += 3) {
-    uint4 raw[3][2], wq[3];
+  const int h = HH * info[IT_HALF] + hs;
+  const bool hv = h < P.h_q;
+  const uint16_t* qh = P.q + ((size_t)info[IT_TOKEN] * P.h_q + (hv ? h : 0)) * D_QK + 8 * chn;
+  const uint16_t* wp = P.norm_w + 8 * chn;
+  const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  uint4 raw[9];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+  for (int a = 0; a < 9; ++a) raw[a] = hv ? ldg_nc(qh + 64 * a) : make_uint4(0, 0, 0, 0);
+  // pass 1: sum of squares of q, largest |q * w|
+  float ss = 0.f, amax = 0.f;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int h = hs + 32 * k;
-        raw[j][k] = (h < P.h_q) ? ldg_nc(qt + (size_t)h * D_QK + 64 * (a0 + j) + 8 * chn) : make_uint4(0, 0, 0, 0);
-      }
-      wq[j] = ldg_nc(P.norm_w + 64 * (a0 + j) + 8 * chn);
-    }
+  for (int a = 0; a < 9; ++a) {
+    const uint4 wq = ldg_nc(wp + 64 * a);
+    const uint32_t x4[4] = {raw[a].x, raw[a].y, raw[a].z, raw[a].w};
+    const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int a = a0 + j;
-      const uint32_t w4[4] = {wq[j].x, wq[j].y, wq[j].z, wq[j].w};
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint4 cu = raw[j][k];
-        const int h = hs + 32 * k;
-        const uint32_t x4[4] = {cu.x, cu.y, cu.z, cu.w};
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
-          ss[k] = fmaf(x0, x0, fmaf(x1, x1, ss[k]));
-          x[2 * e] = x0 * __uint_as_float(w4[e] << 16);
-          x[2 * e + 1] = x1 * __uint_as_float(w4[e] & 0xFFFF0000u);
-        }
-        if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 cs = rope[4 * chn + e];
-            const float x0 = x[2 * e], x1 = x[2 * e + 1];
-            x[2 * e] = x0 * cs.x - x1 * cs.y;
-            x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
-          }
-        }
-        const uint4 o = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                   pack_f16x2(x[6], x[7]));
-        sts128(c.sb + SM_Q + a * 8192 + (h >> 3) * 1024 + (h & 7) * 128 + ((chn ^ (h & 7)) << 4), o);
-      }
-      if ((a & 1) == 1 || a == 8) {
-        // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
-        fence_async_smem();
-        mbar_arrive(bar(c, B_QRDY + (a >> 1)));
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
+      ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+      amax = fmaxf(amax, fmaxf(fabsf(x0 * __uint_as_float(w4[e] << 16)),
+                               fabsf(x1 * __uint_as_float(w4[e] & 0xFFFF0000u))));
     }
   }
-  // per-head statistics: eight lanes hold the pieces of head hs + 32 k
-  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 64 * b;
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  const int ea = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // floor(log2 amax) + 127 (normal amax)
+  int k = ea == 0 ? 0 : 140 - ea;
+  k = k < -100 ? -100 : (k > 100 ? 100 : k);
+  const float sk = __uint_as_float((uint32_t)(127 + k) << 23);     // 2^k, exact
+  // pass 2: the hi / lo operand rows (unrolled: raw[] stays in registers)
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    float v = ss[k];
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    const int h = hs + 32 * k;
-    if (chn == 0) s_inv[h] = (h < P.h_q) ? rsqrtf(v * (1.0f / D_QK) + P.eps) * P.c2 : 0.f;
+  for (int a = 0; a < 9; ++a) {
+    const uint4 wq = ldg_nc(wp + 64 * a);
+    const uint32_t x4[4] = {raw[a].x, raw[a].y, raw[a].z, raw[a].w};
+    const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = __uint_as_float(x4[e] << 16) * __uint_as_float(w4[e] << 16) * sk;
+      x[2 * e + 1] = __uint_as_float(x4[e] & 0xFFFF0000u) * __uint_as_float(w4[e] & 0xFFFF0000u) * sk;
+    }
+    if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 cs = rope[4 * chn + e];
+        const float x0 = x[2 * e], x1 = x[2 * e + 1];
+        x[2 * e] = x0 * cs.x - x1 * cs.y;
+        x[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+      }
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_f16x2(x[2 * e], x[2 * e + 1], hw[e], lw[e]);
+    const uint32_t atom = c.sb + SM_Q + (uint32_t)a * 8192 + ((uint32_t)chn ^ (uint32_t)(hs & 7)) * 16u;
+    sts128(atom + (uint32_t)(hs >> 3) * 1024 + (uint32_t)(hs & 7) * 128, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(atom + (uint32_t)((HH + hs) >> 3) * 1024 + (uint32_t)(hs & 7) * 128, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+    if ((a & 1) == 1 || a == 8) {
+      // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
+      fence_async_smem();
+      mbar_arrive(bar(c, B_QRDY + (a >> 1)));
+    }
   }
+  float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 32 * b;
+  if (chn == 0) s_inv[hs] = hv ? rsqrtf(ss * (1.0f / D_QK) + P.eps) * P.c2 * __uint_as_float((uint32_t)(127 - k) << 23)
+                               : 0.f;
   mbar_arrive(bar(c, B_QSTAT + b));
 }
 
 // ================================================================== DQ
 // Lane (sub, ch) of warp w converts 16 bytes (16 dims) of rows 16 w + 4 k + sub,
 // k = 0..3, per 128-dim chunk: eight lanes read 128 contiguous bytes of a row.  The
-// fp16 values go straight into the 128-byte-swizzled tile (rows of 128 bytes holding 64
+// fp16 codes go straight into the 128-byte-swizzled tile (rows of 128 bytes holding 64
 // dims); the four rows of one store instruction alternate in row parity, which keeps the
-// stores free of bank conflicts.  Raw bytes are loaded two chunks ahead of their
-// conversion (chunk c of a tile lives in register slot c % 2).
+// stores free of bank conflicts.  Chunks are converted in the QK^T order (0, 2, 1, 3);
+// raw bytes are loaded two chunks ahead of their conversion (position p of a tile lives
+// in register slot p % 2).
 // An entry for a row past the end of the item: no list entry has every bit set, since
 // pools hold fewer than 2^31 rows.
 constexpr uint32_t NO_ROW = 0xFFFFFFFFu;
 struct DqRows {
   uint32_t e[4];   // list entries of rows 16 w + 4 k + sub, or NO_ROW
-  uint32_t es;     // lanes ch < 4: entry of row 16 w + 4 ch + sub (its scales), or NO_ROW
 };
 
-DSA_DEV void dq_load_rows(const uint32_t* list, int tt, int nrows, int w, int sub, int ch, DqRows& R) {
+DSA_DEV void dq_load_rows(const uint32_t* list, int tt, int nrows, int w, int sub, DqRows& R) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int r = tt * TILE + 16 * w + 4 * k + sub;
     R.e[k] = r < nrows ? __ldcg(list + r) : NO_ROW;
   }
-  const int rs = tt * TILE + 16 * w + 4 * (ch & 3) + sub;
-  R.es = (ch < 4 && rs < nrows) ? __ldcg(list + rs) : NO_ROW;
 }
 
 DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const DqRows& R, int ch) {
@@ -568,17 +650,12 @@ DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const Dq
     dst[k] = R.e[k] != NO_ROW ? ldg_nc(row_ptr(P, R.e[k]) + 128 * cidx + 16 * ch) : make_uint4(0, 0, 0, 0);
 }
 
-DSA_DEV uint4 dq_load_scales(const KParams& P, const DqRows& R) {
-  return R.es != NO_ROW ? ldg_nc(row_ptr(P, R.es) + D_LAT) : make_uint4(0, 0, 0, 0);
-}
-
 DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int lane) {
   const int sub = lane >> 3, ch = lane & 7;
   const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
   const uint32_t c0 = (uint32_t)(2 * (ch & 3));
   const uint32_t pa = c0 + (uint32_t)(ch >> 2), pb = c0 + 1 - (uint32_t)(ch >> 2);   // 16-byte chunks of the two stores
   uint4 raw[2][4];
-  uint4 scl;
   DqRows cur, nxt;
   uint32_t g = 0, seq = 0;
   // Without splits the dequant warps finish column blocks 1 (warps 0-3) and 2 (warps
@@ -590,15 +667,17 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
   uint32_t pend_nq = 0;   // its index among the items with tiles
   uint32_t nq = 0;
   auto do_share = [&]() -> bool {
-    const int pb = pend % NB;
+    const int pbf = pend % NB;
     if (!wait_bar_w(c, B_ODONE, pend_nq & 1)) return false;
     if (!wait_bar_w(c, B_LREADY, pend_nq & 1)) return false;
     tc_fence_after();
     const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
-    const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * pb;
-    epi_chunk<8>(c, tmem, w & 3, lane, 1 + (w >> 2), reinterpret_cast<const float*>(c.sm + SM_EL), O,
-                 item_info(c, pb)[IT_TOKEN], nullptr, rope);
-    mbar_arrive(bar(c, B_ITEMPTY + pb));
+    const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * pbf;
+    const int* pinfo = item_info(c, pbf);
+    const int cidx = 1 + (w >> 2);
+    epi_chunk<8>(c, tmem, w & 3, lane, cidx, reinterpret_cast<const float*>(c.sm + SM_EL), item_ref(c, pbf)[cidx],
+                 O, pinfo[IT_TOKEN], HH * pinfo[IT_HALF], nullptr, rope);
+    mbar_arrive(bar(c, B_ITEMPTY + pbf));
     pend = -1;
     return true;
   };
@@ -614,10 +693,9 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       if (info[IT_T] > 0) {
         if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
         build_q(qa, c, b, 32 * w + lane);
-        dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, ch, cur);
-        scl = dq_load_scales(P, cur);
-        dq_load_chunk(P, raw[0], 0, cur, ch);
-        dq_load_chunk(P, raw[1], 1, cur, ch);
+        dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, cur);
+        dq_load_chunk(P, raw[0], qk_chunk(0), cur, ch);
+        dq_load_chunk(P, raw[1], qk_chunk(1), cur, ch);
         return 1;
       }
       mbar_arrive(bar(c, B_QSTAT + b));   // no q~: the phase still follows the buffer's uses
@@ -638,31 +716,31 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       // already out), to be prefetched into L2 one tile ahead of their loads
       bool pf = more;
       if (more) {
-        dq_load_rows(list, tt + 1, nrows, w, sub, ch, nxt);
+        dq_load_rows(list, tt + 1, nrows, w, sub, nxt);
       } else {
         const int nb = (seq + 1) % NB;
         if (__all_sync(0xFFFFFFFFu, mbar_try(bar(c, B_ITFULL + nb), ((seq + 1) / NB) & 1))) {
           const int* ni = item_info(c, nb);
           if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
-            dq_load_rows(item_list(P, nb) + ni[IT_ROW0], 0, ni[IT_NROWS], w, sub, ch, nxt);
+            dq_load_rows(item_list(P, nb) + ni[IT_ROW0], 0, ni[IT_NROWS], w, sub, nxt);
             pf = true;
           }
         }
       }
 #pragma unroll
-      for (int cidx = 0; cidx < 4; ++cidx) {
-        if (!wait_bar_w(c, B_VFREE + cidx, (g & 1) ^ 1)) return;
+      for (int pos = 0; pos < 4; ++pos) {
+        const int cidx = qk_chunk(pos);
+        // the previous tile's PV has read this chunk (and the P block it held)
+        if (!wait_bar_w(c, B_PVD + chunk_free_event(cidx), (g & 1) ^ 1)) return;
         const uint32_t cbase = c.sb + SM_V + (uint32_t)cidx * 32768 + half_off;
-        const uint32_t sc = cidx == 0 ? scl.x : cidx == 1 ? scl.y : cidx == 2 ? scl.z : scl.w;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float sv = __uint_as_float(__shfl_sync(0xFFFFFFFFu, sc, sub * 8 + k));
           // lanes of the second 64-dim atom (ch >= 4) store their upper eight dims first:
           // the eight lanes of a row then hit eight distinct 16-byte bank groups
-          const uint4 rw = raw[cidx & 1][k];
+          const uint4 rw = raw[pos & 1][k];
           const uint4 rr = ch >= 4 ? make_uint4(rw.z, rw.w, rw.x, rw.y) : rw;
           uint32_t o[8];
-          dequant16(rr, __float2half2_rn(sv), o);
+          codes16_to_f16(rr, o);
           const uint32_t row = (uint32_t)(16 * w + 4 * k + sub);
           const uint32_t rsw = row & 7;
           const uint32_t rb = cbase + (row >> 3) * 1024 + rsw * 128;
@@ -671,23 +749,20 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
         }
         fence_async_smem();
         mbar_arrive(bar(c, B_VFULL + cidx));
-        if (cidx == 0 && pf && ch < 6) {
+        if (pos == 0 && pf && ch < 6) {
           // the six 128-byte lines of each next row, one line per lane
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             if (nxt.e[k] != NO_ROW) prefetch_line_l2(row_ptr(P, nxt.e[k]) + 128 * ch);
         }
-        // the chunk two ahead
-        if (cidx < 2) {
-          dq_load_chunk(P, raw[cidx & 1], cidx + 2, cur, ch);
+        // the chunk two positions ahead
+        if (pos < 2) {
+          dq_load_chunk(P, raw[pos & 1], qk_chunk(pos + 2), cur, ch);
         } else if (more) {
-          dq_load_chunk(P, raw[cidx & 1], cidx - 2, nxt, ch);
+          dq_load_chunk(P, raw[pos & 1], qk_chunk(pos - 2), nxt, ch);
         }
       }
-      if (more) {
-        scl = dq_load_scales(P, nxt);
-        cur = nxt;
-      }
+      if (more) cur = nxt;
       ++g;
       if (tt == 0 && pend >= 0 && !do_share()) return;
     }
@@ -716,16 +791,13 @@ DSA_DEV uint64_t dadd(uint64_t d, uint32_t bytes) {
 }
 
 DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
-  constexpr uint32_t IDESC_QK = idesc_f16(128, HP, 0, 0);
-  constexpr uint32_t IDESC_PV = idesc_f16(128, HP, 1, 1);
-  constexpr uint32_t IDESC_L = idesc_f16(128, HP, 0, 1);
+  constexpr uint32_t IDESC_QK = idesc_f16(128, NQ, 0, 0);
+  constexpr uint32_t IDESC_PV = idesc_f16(128, NQ, 1, 1);
   // every descriptor of the loop is one of these plus a constant offset
-  const uint64_t d_k = sdesc(c.sb + SM_V, 16, 1024);        // latent tile, K-major (QK^T)
-  const uint64_t d_v = sdesc(c.sb + SM_V, 16384, 1024);     // latent tile, MN-major (PV)
-  const uint64_t d_q = sdesc(c.sb + SM_Q, 16, 1024);        // q~
-  const uint64_t d_p = sdesc(c.sb + SM_P, 16384, 1024);     // P
-  const uint64_t d_one = sdesc_noswz(c.sb + SM_ONES, 128, 256);
-  uint32_t g = 0, nq = 0;
+  const uint64_t d_k = sdesc(c.sb + SM_V, 16, 1024);        // codes tile, K-major (QK^T)
+  const uint64_t d_v = sdesc(c.sb + SM_V, 16384, 1024);     // codes tile, MN-major (PV)
+  const uint64_t d_q = sdesc(c.sb + SM_Q, 16, 1024);        // q~ hi / lo
+  uint32_t g = 0, nq = 0, np = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq % NB;
     if (!wait_bar(c, B_ITFULL + b, (seq / NB) & 1)) return;
@@ -736,54 +808,60 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
     if (item < 0) return;
     if (T == 0) continue;
     for (int tt = 0; tt < T; ++tt) {
-      // ---- S^T = K~ . q~^T
-      const uint32_t sb = g & 1;
-      const uint32_t d_s = tmem + TM_S + 64 * sb;
-      if (!wait_bar(c, B_SFREE + sb, ((g >> 1) & 1) ^ 1)) return;
-      // chunk loop not unrolled: a smaller issue loop misses the instruction caches less,
-      // which the one issuing thread would otherwise stall on
+      // ---- partial scores T_p = codes_p . q~_p^T, one per latent chunk, then the rope part
+      // (chunk loop not unrolled: a smaller issue loop misses the instruction caches less,
+      // which the one issuing thread would otherwise stall on)
 #pragma unroll 1
-      for (int cidx = 0; cidx < 4; ++cidx) {
-        // q~ chunk (first tile of an item) and the latent chunk of this tile
+      for (int p = 0; p < 4; ++p) {
+        const int cidx = qk_chunk(p);
+        const uint32_t sbf = np % NSB;
+        if (!wait_bar(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
         if (tt == 0 && !wait_bar(c, B_QRDY + cidx, nq & 1)) return;
         if (!wait_bar(c, B_VFULL + cidx, g & 1)) return;
         tc_fence_after();
+        const uint32_t d_s = tmem + TM_S + 64 * sbf;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
           const uint32_t boff = (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
-          mma_ss(d_s, dadd(d_k, aoff), dadd(d_q, boff), IDESC_QK, (cidx | kk) ? 1u : 0u);
+          mma_ss(d_s, dadd(d_k, aoff), dadd(d_q, boff), IDESC_QK, kk ? 1u : 0u);
         }
+        tc_commit(bar(c, B_SFULL + sbf));
+        ++np;
       }
-      if (tt == 0 && !wait_bar(c, B_QRDY + 4, nq & 1)) return;
-      if (!wait_bar(c, B_KRFULL + sb, (g >> 1) & 1)) return;
-      tc_fence_after();
+      {
+        const uint32_t sbf = np % NSB;
+        const uint32_t kb = g & 1;
+        if (!wait_bar(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
+        if (tt == 0 && !wait_bar(c, B_QRDY + 4, nq & 1)) return;
+        if (!wait_bar(c, B_KRFULL + kb, (g >> 1) & 1)) return;
+        tc_fence_after();
+        const uint32_t d_s = tmem + TM_S + 64 * sbf;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ts(d_s, tmem + TM_KR + 32 * sb + 8 * kk, dadd(d_q, 8 * 8192 + kk * 32), IDESC_QK, 1u);
-      tc_commit(bar(c, B_SFULL + sb));
-      tc_commit(bar(c, B_KRFREE + sb));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(d_s, tmem + TM_KR + 32 * kb + 8 * kk, dadd(d_q, 8 * 8192 + kk * 32), IDESC_QK, kk ? 1u : 0u);
+        tc_commit(bar(c, B_SFULL + sbf));
+        tc_commit(bar(c, B_KRFREE + kb));
+        ++np;
+      }
       if (tt == T - 1) tc_commit(bar(c, B_QFREE));   // q~ may be rebuilt after these MMAs
-      // ---- O^T += V~^T . P, l += 1^T . P
-      if (!wait_bar(c, B_PFULL, g & 1)) return;
-      tc_fence_after();
-      const uint32_t first = tt == 0 ? 0u : 1u;
+      // ---- O^T_b += codes_b^T . P_b, one block of output dims per latent block
 #pragma unroll 1
-      for (int cidx = 0; cidx < 4; ++cidx) {
+      for (int pb = 0; pb < 4; ++pb) {
+        if (!wait_bar(c, B_PFULL + pb, g & 1)) return;
+        tc_fence_after();
         if (tt == 0 && nq > 0) {
-          // the previous item's epilogue has read this part of O^T (and l)
-          if (!wait_bar(c, B_OFREE + cidx, (nq - 1) & 1)) return;
+          // the previous item's epilogue has read this part of O^T
+          if (!wait_bar(c, B_OFREE + pb, (nq - 1) & 1)) return;
           tc_fence_after();
         }
+        const uint64_t d_p = sdesc(c.sb + p_buffer(pb), 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + TM_O + 64 * cidx, dadd(d_v, cidx * 32768 + kk * 2048), dadd(d_p, kk * 2048), IDESC_PV,
-                 kk == 0 ? first : 1u);
-        tc_commit(bar(c, B_VFREE + cidx));
+          mma_ss(tmem + TM_O + 64 * pb, dadd(d_v, pb * 32768 + kk * 2048), dadd(d_p, kk * 2048), IDESC_PV,
+                 (tt > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(c, B_PVD + pb));
       }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + TM_L, d_one, dadd(d_p, kk * 2048), IDESC_L, kk == 0 ? first : 1u);
-      tc_commit(bar(c, B_PFREE));
       if (tt == T - 1) tc_commit(bar(c, B_ODONE));
       ++g;
     }
@@ -792,22 +870,27 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
 }
 
 // ================================================================== SM
-// One row of the tile per thread (TMEM lane = row).  Softmax of tile g, then the
-// rotary part of the keys of the next tile, which QK^T needs after PV of tile g.
+// One row of the tile per thread (TMEM lane = row).  The rotary part of a tile's keys
+// (bf16 -> fp16 into TMEM, the A operand of the rope partial) and the row's four block
+// scales, read one tile ahead of their use.
 DSA_DEV void sm_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
-                     int nrows, int r, uint32_t gk) {
+                     int nrows, int r, uint32_t gk, float (&scl)[4]) {
   const bool valid = tt * TILE + r < nrows;
-  uint4 raw[8];
-  const uint8_t* src = valid ? row_ptr(P, __ldcg(list + tt * TILE + r)) + D_LAT + 16 : nullptr;
+  uint4 raw[9];
+  const uint8_t* src = valid ? row_ptr(P, __ldcg(list + tt * TILE + r)) + D_LAT : nullptr;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) raw[k] = valid ? ldg_nc(src + 16 * k) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 9; ++k) raw[k] = valid ? ldg_nc(src + 16 * k) : make_uint4(0, 0, 0, 0);
+  scl[0] = __uint_as_float(raw[0].x);
+  scl[1] = __uint_as_float(raw[0].y);
+  scl[2] = __uint_as_float(raw[0].z);
+  scl[3] = __uint_as_float(raw[0].w);
   uint32_t v[32];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    v[4 * k + 0] = bf16x2_to_f16x2(raw[k].x);
-    v[4 * k + 1] = bf16x2_to_f16x2(raw[k].y);
-    v[4 * k + 2] = bf16x2_to_f16x2(raw[k].z);
-    v[4 * k + 3] = bf16x2_to_f16x2(raw[k].w);
+    v[4 * k + 0] = bf16x2_to_f16x2(raw[k + 1].x);
+    v[4 * k + 1] = bf16x2_to_f16x2(raw[k + 1].y);
+    v[4 * k + 2] = bf16x2_to_f16x2(raw[k + 1].z);
+    v[4 * k + 3] = bf16x2_to_f16x2(raw[k + 1].w);
   }
   const uint32_t kb = gk & 1;
   if (!wait_bar_w(c, B_KRFREE + kb, ((gk >> 1) & 1) ^ 1)) return;
@@ -818,6 +901,21 @@ DSA_DEV void sm_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tla
   mbar_arrive(bar(c, B_KRFULL + kb));
 }
 
+// P_b = P * scale_b / reference_b of row r as hi / lo fp16 into the row of the MN-major B
+// operand at `base` (16-byte chunks 0..3: hi of heads 8q..8q+7, chunks 4..7: their lo).
+DSA_DEV void store_pb(uint32_t base, int r, const float (&p)[HH], float f) {
+  const uint32_t prow = base + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+  const uint32_t rsw = (uint32_t)(r & 7);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_f16x2(p[8 * q + 2 * e] * f, p[8 * q + 2 * e + 1] * f, hw[e], lw[e]);
+    sts128(prow + (((uint32_t)q ^ rsw) << 4), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(prow + ((((uint32_t)q + 4u) ^ rsw) << 4), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+  }
+}
+
 DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
   const int r = q4 * 32 + lane;
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
@@ -825,10 +923,11 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
   float* s_alpha = reinterpret_cast<float*>(c.sm + SM_ALPHA);
   float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
   float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
+  float* s_lw = reinterpret_cast<float*>(c.sm + SM_LW);
   Group grp{B_SMG, 0};
-  uint32_t g = 0, seq = 0, nq = 0;   // tiles, items, items with tiles
-  // next item with tiles: its info waited for, its q~ built (once QK^T of the previous
-  // item has completed) and the rope of its tile 0 converted
+  uint32_t g = 0, seq = 0, nq = 0, np = 0;   // tiles, items, items with tiles, partial scores
+  float scl[4] = {0.f, 0.f, 0.f, 0.f};       // block scales of row r of the next tile
+  // next item with tiles: its info waited for, the rope and scales of its tile 0 loaded
   auto open_item = [&]() -> int {
     while (true) {
       const int b = seq % NB;
@@ -836,7 +935,7 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
-        sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g);
+        sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g, scl);
         return c.misc[M_ABORT] ? -1 : 1;
       }
       mbar_arrive(bar(c, B_ITEMPTY + b));
@@ -849,72 +948,67 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
     const int* info = item_info(c, b);
     const int T = info[IT_T], nrows = info[IT_NROWS];
     const uint32_t* list = item_list(P, b) + info[IT_ROW0];
+    const float* iref = item_iref(c, b);
     // the next item's q into L2 when its info is already out
     {
       const int nb = (seq + 1) % NB;
       if (__all_sync(0xFFFFFFFFu, mbar_try(bar(c, B_ITFULL + nb), ((seq + 1) / NB) & 1))) {
         const int* ni = item_info(c, nb);
         if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
-          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + (size_t)ni[IT_TOKEN] * P.h_q * D_QK);
-          for (int l = r; l < P.h_q * 9; l += N_SM) prefetch_line_l2(qn + 128 * l);
+          const int h0 = HH * ni[IT_HALF];
+          const int nh = (P.h_q - h0) < HH ? (P.h_q - h0) : HH;
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + ((size_t)ni[IT_TOKEN] * P.h_q + h0) * D_QK);
+          for (int l = r; l < nh * 9; l += N_SM) prefetch_line_l2(qn + 128 * l);
         }
       }
     }
-    // the per-head factor of the scores (scale * log2(e) / rms(q)), written with q~ (one
-    // phase of QSTAT[b] per use of item buffer b: the next needs this buffer released)
+    // the per-head factor of the scores (scale * log2(e) / (rms(q) 2^k)), written with q~
+    // (one phase of QSTAT[b] per use of item buffer b: the next needs this buffer released)
     if (!wait_bar_w(c, B_QSTAT + b, (seq / NB) & 1)) return;
-    const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 64 * b;
-    if (r < 64) s_m[r] = -INFINITY;
+    const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 32 * b;
+    if (r < HH) s_m[r] = -INFINITY;
+    float lw0 = 0.f, lw1 = 0.f;   // this warp's row sums of heads lane/2 and 16 + lane/2
     if (!grp.sync(c)) return;
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
-      const uint32_t sb = g & 1;
-      const uint32_t ts = tmem + tlane + TM_S + 64 * sb;
       const bool valid = r < nrows - tt * TILE;
-      if (!wait_bar_w(c, B_SFULL + sb, (g >> 1) & 1)) return;
-      tc_fence_after();
-      // the P buffer is free once PV of the previous tile has completed (in practice it
-      // has: the tensor core ran that PV before this tile's QK^T)
-      if (!wait_bar_w(c, B_PFREE, (g & 1) ^ 1)) return;
-      const uint32_t prow = c.sb + SM_P + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
-      const uint32_t rsw = (uint32_t)(r & 7);
-      // P = exp2(S - m) in fp16 into row r of the MN-major B operand; returns the largest
-      // S - m of the row, i.e. how far the tile exceeds the reference max
-      auto p_pass = [&]() -> float {
-        float dmax = -INFINITY;
+      const float sc[4] = {scl[0], scl[1], scl[2], scl[3]};
+      // ---- the five partial scores of row r, summed with the block scales
+      float y[HH];
+#pragma unroll
+      for (int h = 0; h < HH; ++h) y[h] = 0.f;
 #pragma unroll 1
-        for (int hq = 0; hq < 4; ++hq) {   // 16 heads at a time
-          uint32_t a[16];
+      for (int p = 0; p < NPART; ++p) {
+        const uint32_t sbf = np % NSB;
+        if (!wait_bar_w(c, B_SFULL + sbf, (np / NSB) & 1)) return;
+        tc_fence_after();
+        const int pc = qk_chunk(p < 4 ? p : 0);
+        const float f = p < 4 ? (pc == 0 ? sc[0] : pc == 1 ? sc[1] : pc == 2 ? sc[2] : sc[3]) : 1.0f;
+        const uint32_t ts = tmem + tlane + TM_S + 64 * sbf;
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t a[16], l[16];
           tmem_ld16(ts + 16 * hq, a);
-          const float4* m4 = reinterpret_cast<const float4*>(s_m + 16 * hq);
-          const float4* f4 = reinterpret_cast<const float4*>(s_inv + 16 * hq);
-          float m[16], fi[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f = m4[q], g2 = f4[q];
-            m[4 * q] = f.x; m[4 * q + 1] = f.y; m[4 * q + 2] = f.z; m[4 * q + 3] = f.w;
-            fi[4 * q] = g2.x; fi[4 * q + 1] = g2.y; fi[4 * q + 2] = g2.z; fi[4 * q + 3] = g2.w;
-          }
+          tmem_ld16(ts + HH + 16 * hq, l);
           tc_wait_ld();
-          uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float x0 = valid ? fmaf(__uint_as_float(a[2 * i]), fi[2 * i], -m[2 * i]) : -INFINITY;
-            const float x1 = valid ? fmaf(__uint_as_float(a[2 * i + 1]), fi[2 * i + 1], -m[2 * i + 1]) : -INFINITY;
-            dmax = fmaxf(dmax, fmaxf(x0, x1));
-            pk[i] = pack_f16x2(exp2f(x0), exp2f(x1));
-          }
-          const uint32_t c0 = (uint32_t)(2 * hq);
-          sts128(prow + ((c0 ^ rsw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-          sts128(prow + (((c0 + 1) ^ rsw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
+          for (int i = 0; i < 16; ++i)
+            y[16 * hq + i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[16 * hq + i]);
         }
-        return dmax;
-      };
+        tc_fence_before();
+        mbar_arrive(bar(c, B_SFREE + sbf));
+        ++np;
+      }
+      // scores in log2 units (without the running max)
+#pragma unroll
+      for (int h = 0; h < HH; ++h) y[h] = valid ? y[h] * s_inv[h] : -INFINITY;
       bool need = tt == 0;
       if (!need) {
-        // optimistic pass with the current reference max; redone below if the tile
-        // exceeds it by more than 2^8 somewhere
-        float dmax = p_pass();
+        // optimistic pass with the current reference max; the tile is redone below if it
+        // exceeds the max by more than 2^8 somewhere
+        float dmax = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < HH; ++h) dmax = fmaxf(dmax, y[h] - s_m[h]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xFFFFFFFFu, dmax, o));
         if (lane == 0) s_flag[4 * (g & 1) + q4] = dmax;
@@ -923,47 +1017,38 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         need = !(fmaxf(fmaxf(fl[0], fl[1]), fmaxf(fl[2], fl[3])) <= 8.0f);
       }
       if (need) {
-        // exact tile max per head, new reference max, rescale factors, P again
-#pragma unroll 1
-        for (int hq = 0; hq < 4; ++hq) {
-          uint32_t a[16];
-          tmem_ld16(ts + 16 * hq, a);
-          const float4* f4 = reinterpret_cast<const float4*>(s_inv + 16 * hq);
-          tc_wait_ld();
+        // exact tile max per head, new reference max, rescale factors
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
           float v[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f = f4[q];
-            v[4 * q] = valid ? __uint_as_float(a[4 * q]) * f.x : -INFINITY;
-            v[4 * q + 1] = valid ? __uint_as_float(a[4 * q + 1]) * f.y : -INFINITY;
-            v[4 * q + 2] = valid ? __uint_as_float(a[4 * q + 2]) * f.z : -INFINITY;
-            v[4 * q + 3] = valid ? __uint_as_float(a[4 * q + 3]) * f.w : -INFINITY;
-          }
+          for (int i = 0; i < 16; ++i) v[i] = y[16 * hq + i];
           reduce16<true>(v, lane);          // lanes 2m, 2m + 1: head 16 hq + m
-          if ((lane & 1) == 0) s_red[q4 * 64 + 16 * hq + (lane >> 1)] = v[0];
+          if ((lane & 1) == 0) s_red[q4 * HH + 16 * hq + (lane >> 1)] = v[0];
         }
         if (!grp.sync(c)) return;
-        if (r < 64) {
-          const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
+        if (r < HH) {
+          const float tm = fmaxf(fmaxf(s_red[r], s_red[HH + r]), fmaxf(s_red[2 * HH + r], s_red[3 * HH + r]));
           const float mo = s_m[r];
           const float mn = fmaxf(mo, tm);
           s_m[r] = mn;
           s_alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
         }
         if (!grp.sync(c)) return;
-        p_pass();
       }
-      tc_fence_before();
-      mbar_arrive(bar(c, B_SFREE + sb));     // S^T fully read
+      // ---- P = exp2(score - m) in fp32
+#pragma unroll
+      for (int h = 0; h < HH; ++h) y[h] = exp2f(y[h] - s_m[h]);
       if (need && tt > 0) {
-        // O^T and l rescaled (PV of the previous tile has completed: PFREE above)
+        // O^T rescaled once PV of the previous tile has completed
+        if (!wait_bar_w(c, B_PVD + 3, (g & 1) ^ 1)) return;
         tc_fence_after();
 #pragma unroll 1
-        for (int j = 0; j < 10; ++j) {
+        for (int j = 0; j < 8; ++j) {
           uint32_t a[32];
-          const uint32_t ta = tmem + tlane + 32 * j;   // columns 0..319: O^T then l
+          const uint32_t ta = tmem + tlane + TM_O + 32 * j;   // block j / 2, hi (j even) or lo
           tmem_ld32(ta, a);
-          const float4* al4 = reinterpret_cast<const float4*>(s_alpha + 32 * (j & 1));
+          const float4* al4 = reinterpret_cast<const float4*>(s_alpha);
           tc_wait_ld();
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -977,14 +1062,46 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         }
         tc_wait_st();
       }
-      if (tt == T - 1 && r < 64) reinterpret_cast<float*>(c.sm + SM_MFIN)[64 * (nq & 1) + r] = s_m[r];
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(c, B_PFULL));
-      if (tt == T - 1) mbar_arrive(bar(c, B_MFIN));   // the item's final reference max
+      // ---- P_b hi / lo for the four PV blocks, each as soon as its buffer is free
+#pragma unroll 1
+      for (int pb = 0; pb < 4; ++pb) {
+        // P_0: the shared buffer, last read by PV(2) of the previous tile; P_1 / P_2: after
+        // PV(0) of this tile (chunk 0 and the shared buffer); P_3: after PV(1) (chunk 1)
+        const int ev = pb == 0 ? 2 : (pb == 3 ? 1 : 0);
+        const uint32_t par = pb == 0 ? ((g & 1) ^ 1) : (g & 1);
+        if (!wait_bar_w(c, B_PVD + ev, par)) return;
+        const float f = (pb == 0 ? sc[0] : pb == 1 ? sc[1] : pb == 2 ? sc[2] : sc[3]) * iref[pb];
+        store_pb(c.sb + p_buffer(pb), r, y, valid ? f : 0.f);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(c, B_PFULL + pb));
+      }
+      // ---- this warp's row sums (lanes 2m, 2m + 1: heads m and 16 + m)
+      {
+        const float a0 = (need && tt > 0) ? s_alpha[lane >> 1] : 1.f;
+        const float a1 = (need && tt > 0) ? s_alpha[16 + (lane >> 1)] : 1.f;
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = valid ? y[16 * hq + i] : 0.f;
+          reduce16<false>(v, lane);
+          if (hq == 0) lw0 = fmaf(lw0, a0, v[0]);
+          else lw1 = fmaf(lw1, a1, v[0]);
+        }
+      }
+      if (tt == T - 1) {
+        if (r < HH) reinterpret_cast<float*>(c.sm + SM_MFIN)[HH * (nq & 1) + r] = s_m[r];
+        if ((lane & 1) == 0) {
+          float* lwb = s_lw + (nq & 1) * 4 * HH + q4 * HH;
+          lwb[lane >> 1] = lw0;
+          lwb[16 + (lane >> 1)] = lw1;
+        }
+        mbar_arrive(bar(c, B_MFIN));   // the item's final reference max and row sums
+      }
       ++g;
       if (tt + 1 < T) {
-        sm_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, g);
+        sm_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, g, scl);
         if (c.misc[M_ABORT]) return;
       }
     }
@@ -997,10 +1114,9 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
 
 // ================================================================== EPI
 // The epilogue reads O^T out of TMEM one dim per lane, 16 heads at a time, and finishes
-// it from registers; each 64-head column block of TMEM is released as soon as it is read.
+// it from registers; each column block of TMEM is released as soon as it is read.
 DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int lane) {
   const int er = e * 32 + lane;
-  const uint32_t tlane = (uint32_t)(e * 32) << 16;
   float* s_el = reinterpret_cast<float*>(c.sm + SM_EL);
   float* s_else = reinterpret_cast<float*>(c.sm + SM_ELSE);
   const float ln2 = 0.69314718055994531f;
@@ -1012,93 +1128,87 @@ DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int 
     if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return;
     const int* info = item_info(c, b);
     if (info[IT_ITEM] < 0) return;
-    const int t = info[IT_TOKEN], split = info[IT_SPLIT], T = info[IT_T];
+    const int t = info[IT_TOKEN], half = info[IT_HALF], split = info[IT_SPLIT], T = info[IT_T];
+    const int h0 = HH * half;
     if (T > 0) {
       if (!wait_bar_w(c, B_ODONE, nq & 1)) return;
       if (!wait_bar_w(c, B_MFIN, nq & 1)) return;
       tc_fence_after();
-      // row sums (every TMEM lane holds all 64) -> 1/l and the LSE
-      if (e == 0) {
-        uint32_t a[32];
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          tmem_ld32(tmem + tlane + TM_L + 32 * hf, a);
-          tc_wait_ld();
-          if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s_el[32 * hf + i] = __uint_as_float(a[i]);
-          }
-        }
-      }
-      if (!grp.sync(c)) return;
-      if (er < 64) {
-        const float l = s_el[er];
-        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[64 * (nq & 1) + er];
+      // row sums (four warp partials per head) -> 1/l and the LSE
+      if (er < HH) {
+        const float* lwb = reinterpret_cast<const float*>(c.sm + SM_LW) + (nq & 1) * 4 * HH + er;
+        const float l = (lwb[0] + lwb[HH]) + (lwb[2 * HH] + lwb[3 * HH]);
+        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[HH * (nq & 1) + er];
         const bool any = l > 0.f;
         s_else[er] = any ? mfin + log2f(l) : -INFINITY;
         s_el[er] = any ? 1.f / l : 0.f;
       }
       if (!grp.sync(c)) return;
-      if (!is_split && P.out_lse && er < P.h_q) P.out_lse[(size_t)t * P.h_q + er] = s_else[er] * ln2;
-      if (is_split && er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = s_else[er];
+      if (!is_split && P.out_lse && er < HH && h0 + er < P.h_q) P.out_lse[(size_t)t * P.h_q + h0 + er] = s_else[er] * ln2;
+      if (is_split && er < HH) P.part_lse[((size_t)t * P.n_splits + split) * 64 + h0 + er] = s_else[er];
       const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
       // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
       // is out; one call site for the blocks keeps the finish code in one copy
       if (!is_split) mbar_arrive(bar(c, B_LREADY));
-      float* part = is_split ? P.part_o + ((size_t)t * P.n_splits + split) * HP * D_LAT : nullptr;
+      float* part = is_split ? P.part_o + (((size_t)t * P.n_splits + split) * 64 + h0) * D_LAT : nullptr;
       const int nblk = is_split ? 4 : 2;
+      const float* ref = item_ref(c, b);
 #pragma unroll 1
-      for (int bi = 0; bi < nblk; ++bi)
-        epi_chunk<16>(c, tmem, e, lane, is_split ? bi : 3 * bi, s_el, O, t, part, rope);
+      for (int bi = 0; bi < nblk; ++bi) {
+        const int cidx = is_split ? bi : 3 * bi;
+        epi_chunk<16>(c, tmem, e, lane, cidx, s_el, ref[cidx], O, t, h0, part, rope);
+      }
       ++nq;
     } else if (is_split) {
       // a split without a valid column: LSE -inf, so the combine gives it no weight
-      // (on the queue path such tokens never reach this role: the prep warp writes them)
-      if (er < 64) P.part_lse[((size_t)t * P.n_splits + split) * HP + er] = -INFINITY;
+      // (on the queue path such items never reach this role: the prep warp writes them)
+      if (er < HH) P.part_lse[((size_t)t * P.n_splits + split) * 64 + h0 + er] = -INFINITY;
     }
     if (is_split) {
       // this split's partial is out: it counts in, and after the CTA's roles have
-      // finished every split of the token combines one slice of it (one item per CTA on
-      // this path)
+      // finished every split of the (token, half) combines one slice of it (one item per
+      // CTA on this path)
       __threadfence();
       if (!grp.sync(c)) return;
       if (er == 0) {
-        atomicAdd(&P.counters[t], 1u);
+        atomicAdd(&P.counters[(size_t)t * P.n_halves + half], 1u);
         c.misc[M_COMBINE] = 1;
         c.misc[M_TOKEN] = t;
         c.misc[M_SPLIT] = split;
+        c.misc[M_HALF] = half;
       }
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
   }
 }
 
-// Combine of one token's split partials: split `part` of the token takes the slice
+// Combine of one (token, half)'s split partials: split `part` takes the slice
 // part / n_splits of its (head, 32-dim block) units, one unit per thread; weights
 // exp2(lse_s - M) / sum over splits.
-DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int part, int tid) {
-  float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);       // [MAX_SPLITS][64]
-  float* s_lse = s_cw + MAX_SPLITS * 64;                       // [64]
-  float2* s_rope = reinterpret_cast<float2*>(s_lse + 64);      // [32] (cos, sin)
+DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int half, int part, int tid) {
+  float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);       // [MAX_SPLITS][32]
+  float* s_lse = s_cw + MAX_SPLITS * HH;                       // [32]
+  float2* s_rope = reinterpret_cast<float2*>(s_lse + HH);      // [32] (cos, sin)
   const int ns = P.n_splits;
+  const int h0 = HH * half;
   const float ln2 = 0.69314718055994531f;
-  if (tid < 64) {
-    const float* pl = P.part_lse + (size_t)t * ns * HP + tid;
+  if (tid < HH) {
+    const float* pl = P.part_lse + (size_t)t * ns * 64 + h0 + tid;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(pl + s * HP));
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(pl + s * 64));
     float den = 0.f;
     for (int s = 0; s < ns; ++s) {
-      const float w = (M == -INFINITY) ? 0.f : exp2f(__ldcg(pl + s * HP) - M);
-      s_cw[s * 64 + tid] = w;
+      const float w = (M == -INFINITY) ? 0.f : exp2f(__ldcg(pl + s * 64) - M);
+      s_cw[s * HH + tid] = w;
       den += w;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int s = 0; s < ns; ++s) s_cw[s * 64 + tid] *= inv;
+    for (int s = 0; s < ns; ++s) s_cw[s * HH + tid] *= inv;
     s_lse[tid] = den > 0.f ? (M + log2f(den)) * ln2 : -INFINITY;
   }
   __syncthreads();
-  if (part == 0 && P.out_lse && tid < P.h_q) P.out_lse[(size_t)t * P.h_q + tid] = s_lse[tid];
+  if (part == 0 && P.out_lse && tid < HH && h0 + tid < P.h_q) P.out_lse[(size_t)t * P.h_q + h0 + tid] = s_lse[tid];
   // the rotary table of this token, rebuilt (the item buffers are gone)
   if (tid < 32) {
     const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[tid];
@@ -1109,20 +1219,21 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int part, int 
   }
   __syncthreads();
   const float2* rope = s_rope;
-  const int u0 = part * P.h_q * 16 / ns, u1 = (part + 1) * P.h_q * 16 / ns;
+  const int nh = (P.h_q - h0) < HH ? (P.h_q - h0) : HH;
+  const int u0 = part * nh * 16 / ns, u1 = (part + 1) * nh * 16 / ns;
   for (int u = u0 + tid; u < u1; u += NTHREADS) {
-    const int h = u >> 4, blk = u & 15;
+    const int hh = u >> 4, blk = u & 15;
     float v[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = 0.f;
-    const float* base = P.part_o + ((size_t)t * ns * HP + h) * D_LAT + 32 * blk;
+    const float* base = P.part_o + ((size_t)t * ns * 64 + h0 + hh) * D_LAT + 32 * blk;
 #pragma unroll 1
     for (int s = 0; s < ns; s += 2) {
-      const float w0 = s_cw[s * 64 + h];
-      const float w1 = (s + 1 < ns) ? s_cw[(s + 1) * 64 + h] : 0.f;
+      const float w0 = s_cw[s * HH + hh];
+      const float w1 = (s + 1 < ns) ? s_cw[(s + 1) * HH + hh] : 0.f;
       float4 f0[8], f1[8];
-      const float4* src0 = reinterpret_cast<const float4*>(base + (size_t)s * HP * D_LAT);
-      const float4* src1 = reinterpret_cast<const float4*>(base + (size_t)(s + 1) * HP * D_LAT);
+      const float4* src0 = reinterpret_cast<const float4*>(base + (size_t)s * 64 * D_LAT);
+      const float4* src1 = reinterpret_cast<const float4*>(base + (size_t)(s + 1) * 64 * D_LAT);
 #pragma unroll
       for (int k = 0; k < 8; ++k) f0[k] = w0 != 0.f ? __ldcg(src0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -1135,7 +1246,7 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int part, int 
         v[4 * k + 3] = fmaf(w0, f0[k].w, fmaf(w1, f1[k].w, v[4 * k + 3]));
       }
     }
-    finalize_block(OutPtrs{P.out_fp8, P.out_sf, P.out_precast, P.h_q}, v, t, h, 32 * blk, rope);
+    finalize_block(OutPtrs{P.out_fp8, P.out_sf, P.out_precast, P.h_q}, v, t, h0 + hh, 32 * blk, rope);
   }
 }
 
@@ -1220,24 +1331,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(c, B_VFULL + i), N_DQ);
-      mbar_init(bar(c, B_VFREE + i), 1);
+      mbar_init(bar(c, B_PVD + i), 1);
+      mbar_init(bar(c, B_PFULL + i), N_SM);
       mbar_init(bar(c, B_OFREE + i), N_EPI);
+    }
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(bar(c, B_SFULL + i), 1);
+      mbar_init(bar(c, B_SFREE + i), N_SM);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(c, B_KRFULL + i), N_SM);
       mbar_init(bar(c, B_KRFREE + i), 1);
-      mbar_init(bar(c, B_SFULL + i), 1);
-      mbar_init(bar(c, B_SFREE + i), N_SM);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(bar(c, B_ITFULL + i), N_PREP);
       mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SM + N_EPI + 1);
+      mbar_init(bar(c, B_QSTAT + i), N_DQ);
     }
-    mbar_init(bar(c, B_PFULL), N_SM);
-    mbar_init(bar(c, B_PFREE), 1);
     mbar_init(bar(c, B_ODONE), 1);
     for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_DQ);
-    for (int i = 0; i < NB; ++i) mbar_init(bar(c, B_QSTAT + i), N_DQ);
     mbar_init(bar(c, B_QFREE), 1);
     mbar_init(bar(c, B_MFIN), N_SM);
     mbar_init(bar(c, B_LREADY), N_EPI);
@@ -1250,11 +1362,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     c.misc[M_COMBINE] = 0;
   }
   if (warp == W_MMA) tmem_alloc(c.sb + SM_MISC + 4 * M_TMEM, TM_COLS);
-  {
-    uint32_t* ones = reinterpret_cast<uint32_t*>(c.sm + SM_ONES);
-    for (int i = tid; i < 1024; i += NTHREADS) ones[i] = 0x3C003C00u;   // fp16 1.0 pairs
-    fence_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1291,11 +1398,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     tmem_dealloc(tmem, TM_COLS);
   }
   if (P.n_splits > 1 && c.misc[M_COMBINE] && !c.misc[M_ABORT]) {
-    // every split of the token has stored its partial (the splits are co-resident: this
-    // path is a cooperative launch); bounded wait on the token's arrival count
-    const int t = c.misc[M_TOKEN];
+    // every split of the (token, half) has stored its partial (the splits are
+    // co-resident: this path is a cooperative launch); bounded wait on the arrival count
+    const int t = c.misc[M_TOKEN], half = c.misc[M_HALF];
     if (tid == 0) {
-      const volatile uint32_t* cnt = P.counters + t;
+      const volatile uint32_t* cnt = P.counters + (size_t)t * P.n_halves + half;
       const unsigned long long start = clock64();
       while (*cnt < (uint32_t)P.n_splits) {
         __nanosleep(64);
@@ -1308,7 +1415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
       __threadfence();
     }
     __syncthreads();
-    if (!c.misc[M_ABORT]) combine_token(P, c, t, c.misc[M_SPLIT], tid);
+    if (!c.misc[M_ABORT]) combine_token(P, c, t, half, c.misc[M_SPLIT], tid);
   }
 }
 
@@ -1317,30 +1424,34 @@ struct Layout {
   size_t status_off, work_off, counters_off, lists_off, part_o_off, part_lse_off, total;
 };
 
-static int pick_splits(int s_q, int topk, int num_sms) {
+static int halves_for(int h_q) { return h_q > HH ? 2 : 1; }
+
+static int pick_splits(int s_q, int h_q, int topk, int num_sms) {
   if (s_q <= 0) return 1;
   const int tiles = (topk + TILE - 1) / TILE;
-  if (tiles <= 1 || s_q >= num_sms) return 1;
-  int sp = num_sms / s_q;
+  const long long base = (long long)s_q * halves_for(h_q);
+  if (tiles <= 1 || base >= num_sms) return 1;
+  int sp = (int)(num_sms / base);
   if (sp > tiles) sp = tiles;
   if (sp > MAX_SPLITS) sp = MAX_SPLITS;
   return sp < 1 ? 1 : sp;
 }
 
-static Layout layout_for(int s_q, int n_splits, int num_sms) {
+static Layout layout_for(int s_q, int h_q, int n_splits, int num_sms) {
   Layout L;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   L.status_off = 0;
   L.work_off = 4;
   L.counters_off = 256;
-  size_t off = up(L.counters_off + 4 * (size_t)(s_q > 0 ? s_q : 1));
+  // one int32 per (token, half): the split path's arrival counters, or the queue's order
+  size_t off = up(L.counters_off + 4 * (size_t)(s_q > 0 ? s_q : 1) * halves_for(h_q));
   L.lists_off = off;
   off = up(off + (size_t)num_sms * NB * DSA_MAX_TOPK * 4);
   if (n_splits > 1) {
     L.part_o_off = off;
-    off = up(off + (size_t)s_q * n_splits * HP * D_LAT * 4);
+    off = up(off + (size_t)s_q * n_splits * 64 * D_LAT * 4);
     L.part_lse_off = off;
-    off = up(off + (size_t)s_q * n_splits * HP * 4);
+    off = up(off + (size_t)s_q * n_splits * 64 * 4);
   } else {
     L.part_o_off = L.part_lse_off = 0;
   }
@@ -1384,6 +1495,23 @@ static void rope_turn_table(float base, unsigned long long* out) {
   }
 }
 
+// The fused kernel's dynamic shared-memory limit, raised once per device (any host
+// thread may make the first call).
+static std::mutex g_attr_mutex;
+static bool g_attr_done[DSA_MAX_DEVICES];
+
+static int ensure_smem_attr(int dev) {
+  if (dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (!g_attr_done[dev]) {
+    if (cudaFuncSetAttribute(dsa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
+    g_attr_done[dev] = true;
+  }
+  return DSA_OK;
+}
+
 static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const int32_t* indices,
                   const int32_t* topk_length, const int32_t* positions, const void* norm_w, void* out_fp8,
                   uint8_t* out_sf, float* out_precast, float* lse, const dsa_params* p, void* workspace,
@@ -1396,27 +1524,23 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   if (p->topk > 0 && !indices) return DSA_ERR_INVALID_ARG;
   if ((uses_swa && !kv_swa) || (uses_cmp && !kv_cmp)) return DSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || (kv_swa && !aligned(kv_swa, 16)) || (kv_cmp && !aligned(kv_cmp, 16)) ||
-      !aligned(out_fp8, 16) || !aligned(indices, 4) || !aligned(workspace, 256) || !aligned(norm_w, 2) ||
+      !aligned(out_fp8, 16) || !aligned(indices, 4) || !aligned(workspace, 256) || !aligned(norm_w, 16) ||
       (out_precast && !aligned(out_precast, 16)) || (lse && !aligned(lse, 4)))
     return DSA_ERR_INVALID_ARG;
   int dev = 0;
   const int sms = device_sms(&dev);
   if (sms <= 0) return DSA_ERR_CUDA;
+  if (dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED_DEVICE;
-  const int ns = pick_splits(p->s_q, p->topk, sms);
-  const Layout L = layout_for(p->s_q, ns, sms);
+  const int nh = halves_for(p->h_q);
+  const int ns = pick_splits(p->s_q, p->h_q, p->topk, sms);
+  const Layout L = layout_for(p->s_q, p->h_q, ns, sms);
   if (workspace_bytes < L.total) return DSA_ERR_WORKSPACE_TOO_SMALL;
-
-  static int attr_done[64] = {0};
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(dsa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-        cudaSuccess)
-      return DSA_ERR_CUDA;
-    attr_done[dev] = 1;
-  }
+  rc = ensure_smem_attr(dev);
+  if (rc != DSA_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
   const bool ordered = ns == 1 && p->s_q <= ORDER_MAX_TOKENS;
@@ -1427,7 +1551,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   } else {
     // header and the split arrival counters
-    const size_t n = ns > 1 ? L.counters_off + 4 * (size_t)p->s_q : L.counters_off;
+    const size_t n = ns > 1 ? L.counters_off + 4 * (size_t)p->s_q * nh : L.counters_off;
     if (cudaMemsetAsync(ws, 0, n, st) != cudaSuccess) return DSA_ERR_CUDA;
   }
 
@@ -1460,7 +1584,8 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.rms_eps = p->rms_eps;
   K.flags = p->flags;
   K.n_splits = ns;
-  K.n_items = p->s_q * ns;
+  K.n_halves = nh;
+  K.n_items = p->s_q * nh * ns;
   rope_turn_table(p->rope_base, K.rope_turns);
   const int grid = K.n_items < sms ? K.n_items : sms;
   cudaLaunchConfig_t cfg = {};
@@ -1492,7 +1617,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
 // looked up once per device and cached.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
 static std::mutex g_noalloc_mutex;
-static void* g_noalloc_ptr[64];
+static void* g_noalloc_ptr[DSA_MAX_DEVICES];
 
 static int noalloc_scratch(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -1519,12 +1644,12 @@ static int launch_noalloc(const void* q, const void* kv_swa, const void* kv_cmp,
   int dev = 0;
   const int sms = device_sms(&dev);
   if (sms <= 0) return DSA_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return DSA_ERR_UNSUPPORTED_DEVICE;
+  if (dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED_DEVICE;
-  const Layout L = layout_for(p->s_q, pick_splits(p->s_q, p->topk, sms), sms);
+  const Layout L = layout_for(p->s_q, p->h_q, pick_splits(p->s_q, p->h_q, p->topk, sms), sms);
   if (L.total > (size_t)DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   rc = noalloc_scratch(dev, &scratch);
@@ -1564,7 +1689,7 @@ int dsa_sparse_attn_num_splits(const dsa_params* p, int num_sms) {
   if (dsa::check_params(p) != DSA_OK) return 0;
   if (num_sms <= 0) num_sms = dsa::device_sms(nullptr);
   if (num_sms <= 0) return 0;
-  return dsa::pick_splits(p->s_q, p->topk, num_sms);
+  return dsa::pick_splits(p->s_q, p->h_q, p->topk, num_sms);
 }
 
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms) {
@@ -1572,7 +1697,7 @@ size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms) {
   if (ns <= 0) return 0;
   if (num_sms <= 0) num_sms = dsa::device_sms(nullptr);
   if (num_sms <= 0) return 0;
-  return dsa::layout_for(p->s_q, ns, num_sms).total;
+  return dsa::layout_for(p->s_q, p->h_q, ns, num_sms).total;
 }
 
 int dsa_sparse_attn_fwd(const void* q, const void* kv_swa, const void* kv_cmp, const int32_t* indices,
@@ -1613,7 +1738,8 @@ const char* dsa_error_string(int code) {
     case DSA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (h_q outside [1,64], topk > 2048, pool >= 2^31 rows)";
     case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (see dsa_sparse_attn_workspace_size)";
     case DSA_ERR_CUDA: return "CUDA runtime error";
-    case DSA_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case DSA_ERR_UNSUPPORTED_DEVICE:
+      return "current device is not compute capability 10.3 (GB300), or its ordinal is >= DSA_MAX_DEVICES";
     case DSA_ERR_SCRATCH_LIMIT:
       return "shape needs more scratch than the no-alloc entry's built-in DSA_NOALLOC_SCRATCH_BYTES";
     default: return "unknown error";

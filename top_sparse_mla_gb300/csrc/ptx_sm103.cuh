@@ -161,24 +161,32 @@ DSA_DEV void sts128(uint32_t addr, uint4 v) {
 }
 
 // ---------------------------------------------------------------- conversions
-// two E4M3 codes (first value in the low byte) -> f16x2, times an f16x2 scale
-DSA_DEV uint32_t e4m3x2_scaled(uint32_t two_codes, __half2 s2) {
+// two E4M3 codes (first value in the low byte) -> f16x2; every E4M3 value is exact in fp16
+DSA_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)two_codes));
-  __half2 v = *reinterpret_cast<__half2*>(&h);
-  v = __hmul2(v, s2);
-  return *reinterpret_cast<uint32_t*>(&v);
+  return h;
 }
 // 16 E4M3 codes -> 8 f16x2 words
-DSA_DEV void dequant16(uint4 c, __half2 s2, uint32_t* o) {
-  o[0] = e4m3x2_scaled(c.x & 0xFFFF, s2);
-  o[1] = e4m3x2_scaled(c.x >> 16, s2);
-  o[2] = e4m3x2_scaled(c.y & 0xFFFF, s2);
-  o[3] = e4m3x2_scaled(c.y >> 16, s2);
-  o[4] = e4m3x2_scaled(c.z & 0xFFFF, s2);
-  o[5] = e4m3x2_scaled(c.z >> 16, s2);
-  o[6] = e4m3x2_scaled(c.w & 0xFFFF, s2);
-  o[7] = e4m3x2_scaled(c.w >> 16, s2);
+DSA_DEV void codes16_to_f16(uint4 c, uint32_t* o) {
+  o[0] = e4m3x2_to_f16x2(c.x & 0xFFFF);
+  o[1] = e4m3x2_to_f16x2(c.x >> 16);
+  o[2] = e4m3x2_to_f16x2(c.y & 0xFFFF);
+  o[3] = e4m3x2_to_f16x2(c.y >> 16);
+  o[4] = e4m3x2_to_f16x2(c.z & 0xFFFF);
+  o[5] = e4m3x2_to_f16x2(c.z >> 16);
+  o[6] = e4m3x2_to_f16x2(c.w & 0xFFFF);
+  o[7] = e4m3x2_to_f16x2(c.w >> 16);
+}
+// Two fp32 values as fp16 hi + lo pairs: hi = fp16(x) (nearest even), lo = fp16(x - hi).
+// x - hi is exact in fp32, so hi + lo carries x to about 2^-22 relative (exactly when x
+// has at most 16 significant bits and lo is a normal fp16).  First value in the low half.
+DSA_DEV void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 // two bf16 (first in the low half) -> f16x2
 DSA_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {

@@ -25,6 +25,7 @@ DSA_FLAG_TEST_WAIT_TIMEOUT = 2
 DSA_STATUS_INDEX_OUT_OF_RANGE = 1
 DSA_STATUS_WAIT_TIMEOUT = 2
 DSA_MAX_HEADS = 64
+DSA_MAX_DEVICES = 64
 DSA_MAX_TOPK = 2048
 DSA_ORDER_MAX_TOKENS = 65536
 DSA_TOPK_MAX_COLS = 65536
