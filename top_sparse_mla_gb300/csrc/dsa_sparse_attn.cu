@@ -67,10 +67,10 @@ constexpr int ROW_BYTES = 656;
 constexpr int TILE = 128;           // gathered rows per tile (the M of QK^T)
 constexpr int HH = 32;              // heads per work item
 constexpr int NQ = 64;              // N of both contractions: 32 heads hi, then 32 lo
-constexpr int W_SM = 8, W_EPI = 12, W_MMA = 16, W_PREP = 17;
+constexpr int W_SX = 8, W_MMA = 16, W_PREP = 17;
 constexpr int NWARPS = 18;
 constexpr int NTHREADS = 32 * NWARPS;
-constexpr int N_DQ = 256, N_SM = 128, N_EPI = 128, N_PREP = 32;
+constexpr int N_DQ = 256, N_SX = 256, N_PREP = 32;
 constexpr int MAX_SPLITS = 16;
 constexpr int NB = 4;              // item buffers: the prep warp runs up to NB - 1 items ahead
 constexpr int NSB = 3;             // partial-score buffers in TMEM
@@ -91,13 +91,12 @@ constexpr uint32_t SM_INV = SM_ROPE + NB * 256;    // NB x 32 fp32 score factors
 constexpr uint32_t SM_ITEM = SM_INV + NB * 128;    // NB x 16 ints
 constexpr uint32_t SM_M = SM_ITEM + NB * 64;       // 32 fp32 running max (log2 units)
 constexpr uint32_t SM_ALPHA = SM_M + 128;          // 32 fp32 rescale factors
-constexpr uint32_t SM_MFIN = SM_ALPHA + 128;       // 2 x 32 fp32 final max per item
-constexpr uint32_t SM_RED = SM_MFIN + 256;         // 4 warps x 32 fp32
-constexpr uint32_t SM_LW = SM_RED + 512;           // 2 x 4 warps x 32 fp32 row-sum partials
+constexpr uint32_t SM_RED = SM_ALPHA + 128;        // 2 groups x 4 warps x 16 fp32
+constexpr uint32_t SM_LW = SM_RED + 512;           // 2 x 8 warps x 16 fp32 row-sum partials
 constexpr uint32_t SM_EL = SM_LW + 1024;           // 32 fp32 1/l
 constexpr uint32_t SM_ELSE = SM_EL + 128;          // 32 fp32 LSE (log2 units)
-constexpr uint32_t SM_FLAG = SM_ELSE + 128;        // 2 x 4 fp32
-constexpr uint32_t SM_MISC = SM_FLAG + 32;         // misc ints
+constexpr uint32_t SM_FLAG = SM_ELSE + 128;        // 2 groups x 2 x 4 fp32
+constexpr uint32_t SM_MISC = SM_FLAG + 64;         // misc ints
 constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
 constexpr uint32_t SM_END = SM_BAR + 64 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
@@ -108,8 +107,8 @@ constexpr uint32_t SM_CW = SM_V;
 enum {
   B_VFULL = 0, B_PVD = B_VFULL + 4, B_PFULL = B_PVD + 4, B_SFULL = B_PFULL + 4, B_SFREE = B_SFULL + NSB,
   B_KRFULL = B_SFREE + NSB, B_KRFREE = B_KRFULL + 2, B_ITFULL = B_KRFREE + 2, B_ITEMPTY = B_ITFULL + NB,
-  B_ODONE = B_ITEMPTY + NB, B_OFREE, B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_MFIN = B_QSTAT + NB,
-  B_LREADY, B_SMG, B_EPG, B_DRAIN, B_NEVER, B_COUNT
+  B_ODONE = B_ITEMPTY + NB, B_OFREE, B_QRDY = B_OFREE + 4, B_QFREE = B_QRDY + 5, B_QSTAT, B_LREADY = B_QSTAT + NB,
+  B_SXG, B_SXA = B_SXG + 2, B_DRAIN, B_NEVER, B_COUNT
 };
 static_assert(B_COUNT <= 64, "barrier area");
 
@@ -482,26 +481,29 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[N], int t, int h0, int 
 }
 
 // Epilogue of the 128-dim column block cidx of O^T by a warp on TMEM lane quarter q4
-// (dims 128 cidx + 32 q4 + lane), NH heads at a time: (O_hi + O_lo) times the block's
-// reference scale and 1/l from s_il.  The block is released on OFREE[cidx] once it has
-// been read.  With part set the normalised partial is stored instead of finished.
+// (dims 128 cidx + 32 q4 + lane) for the item's heads hb .. hb + NH * ng - 1, NH at a
+// time: (O_hi + O_lo) times the block's reference scale and 1/l from s_il.  The block's
+// share is released on OFREE[cidx] once it has been read.  With part set the normalised
+// partial is stored instead of finished.  (Out of line: its registers would otherwise
+// count against the callers' loops.)
 template <int NH>
-DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, const float* s_il, float ref,
-                       const OutPtrs& O, int t, int h0, float* part, const float2* rope) {
+__device__ __noinline__ void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, int hb, int ng, const float* s_il,
+                       float ref, const OutPtrs& O, int t, int h0, float* part, const float2* rope) {
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
   const int d = 128 * cidx + 32 * q4 + lane;
 #pragma unroll 1
-  for (int hg = 0; hg < HH / NH; ++hg) {
+  for (int hg = 0; hg < ng; ++hg) {
+    const int col = hb + NH * hg;
     uint32_t a[NH], l[NH];
     if constexpr (NH == 16) {
-      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
-      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + HH + NH * hg, l);
+      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + col, a);
+      tmem_ld16(tmem + tlane + TM_O + 64 * cidx + HH + col, l);
     } else {
-      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + NH * hg, a);
-      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + HH + NH * hg, l);
+      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + col, a);
+      tmem_ld8(tmem + tlane + TM_O + 64 * cidx + HH + col, l);
     }
     tc_wait_ld();
-    const float4* il4 = reinterpret_cast<const float4*>(s_il + NH * hg);
+    const float4* il4 = reinterpret_cast<const float4*>(s_il + col);
     float v[NH];
 #pragma unroll
     for (int q = 0; q < NH / 4; ++q) {
@@ -511,16 +513,16 @@ DSA_DEV void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int lane, int cidx, 
       v[4 * q + 2] = (__uint_as_float(a[4 * q + 2]) + __uint_as_float(l[4 * q + 2])) * (ref * f.z);
       v[4 * q + 3] = (__uint_as_float(a[4 * q + 3]) + __uint_as_float(l[4 * q + 3])) * (ref * f.w);
     }
-    if (hg == HH / NH - 1) {
+    if (hg == ng - 1) {
       tc_fence_before();
-      mbar_arrive(bar(c, B_OFREE + cidx));   // this part of O^T has been read
+      mbar_arrive(bar(c, B_OFREE + cidx));   // this share of O^T has been read
     }
     if (part) {
-      float* o = part + (size_t)(NH * hg) * D_LAT + d;
+      float* o = part + (size_t)col * D_LAT + d;
 #pragma unroll
       for (int i = 0; i < NH; ++i) o[(size_t)i * D_LAT] = v[i];
     } else {
-      finalize_lanes<NH>(O, v, t, h0 + NH * hg, d, lane, rope);
+      finalize_lanes<NH>(O, v, t, h0 + col, d, lane, rope);
     }
   }
 }
@@ -675,8 +677,8 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
     const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * pbf;
     const int* pinfo = item_info(c, pbf);
     const int cidx = 1 + (w >> 2);
-    epi_chunk<8>(c, tmem, w & 3, lane, cidx, reinterpret_cast<const float*>(c.sm + SM_EL), item_ref(c, pbf)[cidx],
-                 O, pinfo[IT_TOKEN], HH * pinfo[IT_HALF], nullptr, rope);
+    epi_chunk<8>(c, tmem, w & 3, lane, cidx, 0, HH / 8, reinterpret_cast<const float*>(c.sm + SM_EL),
+                 item_ref(c, pbf)[cidx], O, pinfo[IT_TOKEN], HH * pinfo[IT_HALF], nullptr, rope);
     mbar_arrive(bar(c, B_ITEMPTY + pbf));
     pend = -1;
     return true;
@@ -869,24 +871,27 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   }
 }
 
-// ================================================================== SM
-// One row of the tile per thread (TMEM lane = row).  The rotary part of a tile's keys
-// (bf16 -> fp16 into TMEM, the A operand of the rope partial) and the row's four block
-// scales, read one tile ahead of their use.
-DSA_DEV void sm_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
-                     int nrows, int r, uint32_t gk, float (&scl)[4]) {
+// ================================================================== SX
+// The softmax warps: two groups of four; group gq takes the item's heads 16 gq ..
+// 16 gq + 15 and each of its threads one row of the tile (TMEM lane = row).  Before a
+// tile: the rotary part of its keys (bf16 -> fp16 into TMEM, the A operand of the rope
+// partial; each group converts half of the 64 dims) and the row's four block scales,
+// read one tile ahead of their use.
+DSA_DEV void sx_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
+                     int nrows, int r, int gq, uint32_t gk, float (&scl)[4]) {
   const bool valid = tt * TILE + r < nrows;
-  uint4 raw[9];
   const uint8_t* src = valid ? row_ptr(P, __ldcg(list + tt * TILE + r)) + D_LAT : nullptr;
+  uint4 raw[5];
+  raw[0] = valid ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int k = 0; k < 9; ++k) raw[k] = valid ? ldg_nc(src + 16 * k) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 4; ++k) raw[k + 1] = valid ? ldg_nc(src + 16 + 64 * gq + 16 * k) : make_uint4(0, 0, 0, 0);
   scl[0] = __uint_as_float(raw[0].x);
   scl[1] = __uint_as_float(raw[0].y);
   scl[2] = __uint_as_float(raw[0].z);
   scl[3] = __uint_as_float(raw[0].w);
-  uint32_t v[32];
+  uint32_t v[16];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < 4; ++k) {
     v[4 * k + 0] = bf16x2_to_f16x2(raw[k + 1].x);
     v[4 * k + 1] = bf16x2_to_f16x2(raw[k + 1].y);
     v[4 * k + 2] = bf16x2_to_f16x2(raw[k + 1].z);
@@ -895,38 +900,61 @@ DSA_DEV void sm_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tla
   const uint32_t kb = gk & 1;
   if (!wait_bar_w(c, B_KRFREE + kb, ((gk >> 1) & 1) ^ 1)) return;
   tc_fence_after();
-  tmem_st32(tmem + tlane + TM_KR + 32 * kb, v);
+  tmem_st16(tmem + tlane + TM_KR + 32 * kb + 16 * gq, v);
   tc_wait_st();
   tc_fence_before();
   mbar_arrive(bar(c, B_KRFULL + kb));
 }
 
-// P_b = P * scale_b / reference_b of row r as hi / lo fp16 into the row of the MN-major B
-// operand at `base` (16-byte chunks 0..3: hi of heads 8q..8q+7, chunks 4..7: their lo).
-DSA_DEV void store_pb(uint32_t base, int r, const float (&p)[HH], float f) {
+// P_b = P * scale_b / reference_b of row r for the group's 16 heads, as hi / lo fp16 into
+// the row of the MN-major B operand at `base` (16-byte chunks 2 gq, 2 gq + 1: hi of the
+// group's heads; chunks 4 + 2 gq, 5 + 2 gq: their lo).
+DSA_DEV void store_pb(uint32_t base, int r, int gq, const float (&p)[16], float f) {
   const uint32_t prow = base + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
   const uint32_t rsw = (uint32_t)(r & 7);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int j = 0; j < 2; ++j) {
     uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) split_f16x2(p[8 * q + 2 * e] * f, p[8 * q + 2 * e + 1] * f, hw[e], lw[e]);
-    sts128(prow + (((uint32_t)q ^ rsw) << 4), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-    sts128(prow + ((((uint32_t)q + 4u) ^ rsw) << 4), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+    for (int e = 0; e < 4; ++e) split_f16x2(p[8 * j + 2 * e] * f, p[8 * j + 2 * e + 1] * f, hw[e], lw[e]);
+    const uint32_t q = (uint32_t)(2 * gq + j);
+    sts128(prow + ((q ^ rsw) << 4), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(prow + (((q + 4u) ^ rsw) << 4), make_uint4(lw[0], lw[1], lw[2], lw[3]));
   }
 }
 
-DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int lane) {
+DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int q4, int lane) {
   const int r = q4 * 32 + lane;
+  const int hb = 16 * gq;                       // the group's first head within the item
   const uint32_t tlane = (uint32_t)(q4 * 32) << 16;
   float* s_m = reinterpret_cast<float*>(c.sm + SM_M);
   float* s_alpha = reinterpret_cast<float*>(c.sm + SM_ALPHA);
-  float* s_red = reinterpret_cast<float*>(c.sm + SM_RED);
-  float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG);
-  float* s_lw = reinterpret_cast<float*>(c.sm + SM_LW);
-  Group grp{B_SMG, 0};
+  float* s_red = reinterpret_cast<float*>(c.sm + SM_RED) + 64 * gq;     // 4 warps x 16
+  float* s_flag = reinterpret_cast<float*>(c.sm + SM_FLAG) + 8 * gq;    // 2 x 4
+  float* s_lw = reinterpret_cast<float*>(c.sm + SM_LW);                 // 2 x 8 warps x 16
+  float* s_el = reinterpret_cast<float*>(c.sm + SM_EL);
+  float* s_else = reinterpret_cast<float*>(c.sm + SM_ELSE);
+  const float ln2 = 0.69314718055994531f;
+  const bool is_split = P.n_splits > 1;
+  Group grp{B_SXG + gq, 0};     // the four warps of this group
+  Group all{B_SXA, 0};          // both groups
   uint32_t g = 0, seq = 0, nq = 0, np = 0;   // tiles, items, items with tiles, partial scores
   float scl[4] = {0.f, 0.f, 0.f, 0.f};       // block scales of row r of the next tile
+  // A split of a (token, half) has stored its partial (or its LSE of -inf): it counts
+  // in, and after the CTA's roles have finished every split combines one slice of it
+  // (one item per CTA on this path).
+  auto count_in = [&](int t, int split, int half) -> bool {
+    __threadfence();
+    if (!all.sync(c)) return false;
+    if (gq == 0 && r == 0) {
+      atomicAdd(&P.counters[(size_t)t * P.n_halves + half], 1u);
+      c.misc[M_COMBINE] = 1;
+      c.misc[M_TOKEN] = t;
+      c.misc[M_SPLIT] = split;
+      c.misc[M_HALF] = half;
+    }
+    return true;
+  };
   // next item with tiles: its info waited for, the rope and scales of its tile 0 loaded
   auto open_item = [&]() -> int {
     while (true) {
@@ -935,8 +963,15 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
-        sm_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, g, scl);
+        sx_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, gq, g, scl);
         return c.misc[M_ABORT] ? -1 : 1;
+      }
+      if (is_split) {
+        // a split without a valid column: LSE -inf, so the combine gives it no weight
+        // (on the queue path such items never reach this role: the prep warp writes them)
+        const int t = info[IT_TOKEN], half = info[IT_HALF], split = info[IT_SPLIT];
+        if (r < 16) P.part_lse[((size_t)t * P.n_splits + split) * 64 + HH * half + hb + r] = -INFINITY;
+        if (!count_in(t, split, half)) return -1;
       }
       mbar_arrive(bar(c, B_ITEMPTY + b));
       ++seq;
@@ -947,36 +982,38 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
     const int b = seq % NB;
     const int* info = item_info(c, b);
     const int T = info[IT_T], nrows = info[IT_NROWS];
+    const int t = info[IT_TOKEN], half = info[IT_HALF], split = info[IT_SPLIT];
+    const int h0 = HH * half;
     const uint32_t* list = item_list(P, b) + info[IT_ROW0];
     const float* iref = item_iref(c, b);
     // the next item's q into L2 when its info is already out
-    {
+    if (gq == 0) {
       const int nb = (seq + 1) % NB;
       if (__all_sync(0xFFFFFFFFu, mbar_try(bar(c, B_ITFULL + nb), ((seq + 1) / NB) & 1))) {
         const int* ni = item_info(c, nb);
         if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
-          const int h0 = HH * ni[IT_HALF];
-          const int nh = (P.h_q - h0) < HH ? (P.h_q - h0) : HH;
-          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + ((size_t)ni[IT_TOKEN] * P.h_q + h0) * D_QK);
-          for (int l = r; l < nh * 9; l += N_SM) prefetch_line_l2(qn + 128 * l);
+          const int nh0 = HH * ni[IT_HALF];
+          const int nh = (P.h_q - nh0) < HH ? (P.h_q - nh0) : HH;
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + ((size_t)ni[IT_TOKEN] * P.h_q + nh0) * D_QK);
+          for (int l = r; l < nh * 9; l += 128) prefetch_line_l2(qn + 128 * l);
         }
       }
     }
     // the per-head factor of the scores (scale * log2(e) / (rms(q) 2^k)), written with q~
     // (one phase of QSTAT[b] per use of item buffer b: the next needs this buffer released)
     if (!wait_bar_w(c, B_QSTAT + b, (seq / NB) & 1)) return;
-    const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 32 * b;
-    if (r < HH) s_m[r] = -INFINITY;
-    float lw0 = 0.f, lw1 = 0.f;   // this warp's row sums of heads lane/2 and 16 + lane/2
+    const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 32 * b + hb;
+    if (r < 16) s_m[hb + r] = -INFINITY;
+    float lw = 0.f;   // this warp's row sum of head hb + lane / 2
     if (!grp.sync(c)) return;
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
       const bool valid = r < nrows - tt * TILE;
       const float sc[4] = {scl[0], scl[1], scl[2], scl[3]};
       // ---- the five partial scores of row r, summed with the block scales
-      float y[HH];
+      float y[16];
 #pragma unroll
-      for (int h = 0; h < HH; ++h) y[h] = 0.f;
+      for (int h = 0; h < 16; ++h) y[h] = 0.f;
 #pragma unroll 1
       for (int p = 0; p < NPART; ++p) {
         const uint32_t sbf = np % NSB;
@@ -984,31 +1021,27 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
         tc_fence_after();
         const int pc = qk_chunk(p < 4 ? p : 0);
         const float f = p < 4 ? (pc == 0 ? sc[0] : pc == 1 ? sc[1] : pc == 2 ? sc[2] : sc[3]) : 1.0f;
-        const uint32_t ts = tmem + tlane + TM_S + 64 * sbf;
-#pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-          uint32_t a[16], l[16];
-          tmem_ld16(ts + 16 * hq, a);
-          tmem_ld16(ts + HH + 16 * hq, l);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            y[16 * hq + i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[16 * hq + i]);
-        }
+        const uint32_t ts = tmem + tlane + TM_S + 64 * sbf + hb;
+        uint32_t a[16], l[16];
+        tmem_ld16(ts, a);
+        tmem_ld16(ts + HH, l);
+        tc_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(c, B_SFREE + sbf));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[i]);
         ++np;
       }
       // scores in log2 units (without the running max)
 #pragma unroll
-      for (int h = 0; h < HH; ++h) y[h] = valid ? y[h] * s_inv[h] : -INFINITY;
+      for (int h = 0; h < 16; ++h) y[h] = valid ? y[h] * s_inv[h] : -INFINITY;
       bool need = tt == 0;
       if (!need) {
         // optimistic pass with the current reference max; the tile is redone below if it
         // exceeds the max by more than 2^8 somewhere
         float dmax = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < HH; ++h) dmax = fmaxf(dmax, y[h] - s_m[h]);
+        for (int h = 0; h < 16; ++h) dmax = fmaxf(dmax, y[h] - s_m[hb + h]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xFFFFFFFFu, dmax, o));
         if (lane == 0) s_flag[4 * (g & 1) + q4] = dmax;
@@ -1018,168 +1051,104 @@ DSA_DEV void sm_role(const KParams& P, const Ctx& c, uint32_t tmem, int q4, int 
       }
       if (need) {
         // exact tile max per head, new reference max, rescale factors
+        float v[16];
 #pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = y[16 * hq + i];
-          reduce16<true>(v, lane);          // lanes 2m, 2m + 1: head 16 hq + m
-          if ((lane & 1) == 0) s_red[q4 * HH + 16 * hq + (lane >> 1)] = v[0];
-        }
+        for (int i = 0; i < 16; ++i) v[i] = y[i];
+        reduce16<true>(v, lane);          // lanes 2m, 2m + 1: head hb + m
+        if ((lane & 1) == 0) s_red[q4 * 16 + (lane >> 1)] = v[0];
         if (!grp.sync(c)) return;
-        if (r < HH) {
-          const float tm = fmaxf(fmaxf(s_red[r], s_red[HH + r]), fmaxf(s_red[2 * HH + r], s_red[3 * HH + r]));
-          const float mo = s_m[r];
+        if (r < 16) {
+          const float tm = fmaxf(fmaxf(s_red[r], s_red[16 + r]), fmaxf(s_red[32 + r], s_red[48 + r]));
+          const float mo = s_m[hb + r];
           const float mn = fmaxf(mo, tm);
-          s_m[r] = mn;
-          s_alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+          s_m[hb + r] = mn;
+          s_alpha[hb + r] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
         }
         if (!grp.sync(c)) return;
       }
       // ---- P = exp2(score - m) in fp32
 #pragma unroll
-      for (int h = 0; h < HH; ++h) y[h] = exp2f(y[h] - s_m[h]);
+      for (int h = 0; h < 16; ++h) y[h] = exp2f(y[h] - s_m[hb + h]);
       if (need && tt > 0) {
-        // O^T rescaled once PV of the previous tile has completed
+        // the group's columns of O^T rescaled once PV of the previous tile has completed
         if (!wait_bar_w(c, B_PVD + 3, (g & 1) ^ 1)) return;
         tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j < 8; ++j) {
-          uint32_t a[32];
-          const uint32_t ta = tmem + tlane + TM_O + 32 * j;   // block j / 2, hi (j even) or lo
-          tmem_ld32(ta, a);
-          const float4* al4 = reinterpret_cast<const float4*>(s_alpha);
+          uint32_t a[16];
+          const uint32_t ta = tmem + tlane + TM_O + 64 * (j >> 1) + HH * (j & 1) + hb;   // block j / 2, hi or lo
+          tmem_ld16(ta, a);
           tc_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = al4[q];
-            a[4 * q] = __float_as_uint(__uint_as_float(a[4 * q]) * f.x);
-            a[4 * q + 1] = __float_as_uint(__uint_as_float(a[4 * q + 1]) * f.y);
-            a[4 * q + 2] = __float_as_uint(__uint_as_float(a[4 * q + 2]) * f.z);
-            a[4 * q + 3] = __float_as_uint(__uint_as_float(a[4 * q + 3]) * f.w);
-          }
-          tmem_st32(ta, a);
+          for (int i = 0; i < 16; ++i) a[i] = __float_as_uint(__uint_as_float(a[i]) * s_alpha[hb + i]);
+          tmem_st16(ta, a);
         }
         tc_wait_st();
       }
-      // ---- P_b hi / lo for the four PV blocks, each as soon as its buffer is free
+      // ---- P_b hi / lo for the four PV blocks, each as soon as its buffer is free: P_0 in
+      // the shared buffer (last read by PV(2) of the previous tile), P_1 / P_2 after PV(0)
+      // of this tile (chunk 0, the shared buffer), P_3 after PV(1) (chunk 1).  The row
+      // sums go between P_0 and P_1.
 #pragma unroll 1
       for (int pb = 0; pb < 4; ++pb) {
-        // P_0: the shared buffer, last read by PV(2) of the previous tile; P_1 / P_2: after
-        // PV(0) of this tile (chunk 0 and the shared buffer); P_3: after PV(1) (chunk 1)
         const int ev = pb == 0 ? 2 : (pb == 3 ? 1 : 0);
-        const uint32_t par = pb == 0 ? ((g & 1) ^ 1) : (g & 1);
-        if (!wait_bar_w(c, B_PVD + ev, par)) return;
+        if (!wait_bar_w(c, B_PVD + ev, pb == 0 ? ((g & 1) ^ 1) : (g & 1))) return;
         const float f = (pb == 0 ? sc[0] : pb == 1 ? sc[1] : pb == 2 ? sc[2] : sc[3]) * iref[pb];
-        store_pb(c.sb + p_buffer(pb), r, y, valid ? f : 0.f);
+        store_pb(c.sb + p_buffer(pb), r, gq, y, valid ? f : 0.f);
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(bar(c, B_PFULL + pb));
-      }
-      // ---- this warp's row sums (lanes 2m, 2m + 1: heads m and 16 + m)
-      {
-        const float a0 = (need && tt > 0) ? s_alpha[lane >> 1] : 1.f;
-        const float a1 = (need && tt > 0) ? s_alpha[16 + (lane >> 1)] : 1.f;
-#pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
+        if (pb == 0) {
+          // this warp's row sums (lanes 2m, 2m + 1: head hb + m)
           float v[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = valid ? y[16 * hq + i] : 0.f;
+          for (int i = 0; i < 16; ++i) v[i] = valid ? y[i] : 0.f;
           reduce16<false>(v, lane);
-          if (hq == 0) lw0 = fmaf(lw0, a0, v[0]);
-          else lw1 = fmaf(lw1, a1, v[0]);
+          lw = fmaf(lw, (need && tt > 0) ? s_alpha[hb + (lane >> 1)] : 1.f, v[0]);
         }
-      }
-      if (tt == T - 1) {
-        if (r < HH) reinterpret_cast<float*>(c.sm + SM_MFIN)[HH * (nq & 1) + r] = s_m[r];
-        if ((lane & 1) == 0) {
-          float* lwb = s_lw + (nq & 1) * 4 * HH + q4 * HH;
-          lwb[lane >> 1] = lw0;
-          lwb[16 + (lane >> 1)] = lw1;
-        }
-        mbar_arrive(bar(c, B_MFIN));   // the item's final reference max and row sums
       }
       ++g;
       if (tt + 1 < T) {
-        sm_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, g, scl);
+        sx_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, gq, g, scl);
         if (c.misc[M_ABORT]) return;
+        continue;
       }
+      // ---- the item's last tile: 1/l, LSE and the epilogue of this group's heads
+      if ((lane & 1) == 0) s_lw[(nq & 1) * 128 + (4 * gq + q4) * 16 + (lane >> 1)] = lw;
+      if (!grp.sync(c)) return;
+      if (!wait_bar_w(c, B_ODONE, nq & 1)) return;
+      tc_fence_after();
+      if (r < 16) {
+        const float* lwb = s_lw + (nq & 1) * 128 + 64 * gq + r;
+        const float l = (lwb[0] + lwb[16]) + (lwb[32] + lwb[48]);
+        const bool any = l > 0.f;
+        s_else[hb + r] = any ? s_m[hb + r] + log2f(l) : -INFINITY;
+        s_el[hb + r] = any ? 1.f / l : 0.f;
+      }
+      if (!grp.sync(c)) return;
+      if (r < 16 && h0 + hb + r < P.h_q) {
+        if (is_split) P.part_lse[((size_t)t * P.n_splits + split) * 64 + h0 + hb + r] = s_else[hb + r];
+        else if (P.out_lse) P.out_lse[(size_t)t * P.h_q + h0 + hb + r] = s_else[hb + r] * ln2;
+      }
+      // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
+      // is out
+      if (!is_split) mbar_arrive(bar(c, B_LREADY));
+      const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
+      const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+      float* part = is_split ? P.part_o + (((size_t)t * P.n_splits + split) * 64 + h0) * D_LAT : nullptr;
+      const float* ref = item_ref(c, b);
+      const int nblk = is_split ? 4 : 2;
+#pragma unroll 1
+      for (int bi = 0; bi < nblk; ++bi) {
+        const int cidx = is_split ? bi : 3 * bi;
+        epi_chunk<16>(c, tmem, q4, lane, cidx, hb, 1, s_el, ref[cidx], O, t, h0, part, rope);
+      }
+      if (is_split && !count_in(t, split, half)) return;
     }
     mbar_arrive(bar(c, B_ITEMPTY + b));
     ++seq;
     ++nq;
     if (open_item() <= 0) return;
-  }
-}
-
-// ================================================================== EPI
-// The epilogue reads O^T out of TMEM one dim per lane, 16 heads at a time, and finishes
-// it from registers; each column block of TMEM is released as soon as it is read.
-DSA_DEV void epi_role(const KParams& P, const Ctx& c, uint32_t tmem, int e, int lane) {
-  const int er = e * 32 + lane;
-  float* s_el = reinterpret_cast<float*>(c.sm + SM_EL);
-  float* s_else = reinterpret_cast<float*>(c.sm + SM_ELSE);
-  const float ln2 = 0.69314718055994531f;
-  const bool is_split = P.n_splits > 1;
-  Group grp{B_EPG, 0};
-  uint32_t nq = 0;   // items with tiles
-  for (uint32_t seq = 0;; ++seq) {
-    const int b = seq % NB;
-    if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return;
-    const int* info = item_info(c, b);
-    if (info[IT_ITEM] < 0) return;
-    const int t = info[IT_TOKEN], half = info[IT_HALF], split = info[IT_SPLIT], T = info[IT_T];
-    const int h0 = HH * half;
-    if (T > 0) {
-      if (!wait_bar_w(c, B_ODONE, nq & 1)) return;
-      if (!wait_bar_w(c, B_MFIN, nq & 1)) return;
-      tc_fence_after();
-      // row sums (four warp partials per head) -> 1/l and the LSE
-      if (er < HH) {
-        const float* lwb = reinterpret_cast<const float*>(c.sm + SM_LW) + (nq & 1) * 4 * HH + er;
-        const float l = (lwb[0] + lwb[HH]) + (lwb[2 * HH] + lwb[3 * HH]);
-        const float mfin = reinterpret_cast<const float*>(c.sm + SM_MFIN)[HH * (nq & 1) + er];
-        const bool any = l > 0.f;
-        s_else[er] = any ? mfin + log2f(l) : -INFINITY;
-        s_el[er] = any ? 1.f / l : 0.f;
-      }
-      if (!grp.sync(c)) return;
-      if (!is_split && P.out_lse && er < HH && h0 + er < P.h_q) P.out_lse[(size_t)t * P.h_q + h0 + er] = s_else[er] * ln2;
-      if (is_split && er < HH) P.part_lse[((size_t)t * P.n_splits + split) * 64 + h0 + er] = s_else[er];
-      const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
-      const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
-      // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
-      // is out; one call site for the blocks keeps the finish code in one copy
-      if (!is_split) mbar_arrive(bar(c, B_LREADY));
-      float* part = is_split ? P.part_o + (((size_t)t * P.n_splits + split) * 64 + h0) * D_LAT : nullptr;
-      const int nblk = is_split ? 4 : 2;
-      const float* ref = item_ref(c, b);
-#pragma unroll 1
-      for (int bi = 0; bi < nblk; ++bi) {
-        const int cidx = is_split ? bi : 3 * bi;
-        epi_chunk<16>(c, tmem, e, lane, cidx, s_el, ref[cidx], O, t, h0, part, rope);
-      }
-      ++nq;
-    } else if (is_split) {
-      // a split without a valid column: LSE -inf, so the combine gives it no weight
-      // (on the queue path such items never reach this role: the prep warp writes them)
-      if (er < HH) P.part_lse[((size_t)t * P.n_splits + split) * 64 + h0 + er] = -INFINITY;
-    }
-    if (is_split) {
-      // this split's partial is out: it counts in, and after the CTA's roles have
-      // finished every split of the (token, half) combines one slice of it (one item per
-      // CTA on this path)
-      __threadfence();
-      if (!grp.sync(c)) return;
-      if (er == 0) {
-        atomicAdd(&P.counters[(size_t)t * P.n_halves + half], 1u);
-        c.misc[M_COMBINE] = 1;
-        c.misc[M_TOKEN] = t;
-        c.misc[M_SPLIT] = split;
-        c.misc[M_HALF] = half;
-      }
-    }
-    mbar_arrive(bar(c, B_ITEMPTY + b));
   }
 }
 
@@ -1332,29 +1301,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(c, B_VFULL + i), N_DQ);
       mbar_init(bar(c, B_PVD + i), 1);
-      mbar_init(bar(c, B_PFULL + i), N_SM);
-      mbar_init(bar(c, B_OFREE + i), N_EPI);
+      mbar_init(bar(c, B_PFULL + i), N_SX);
+      // O^T blocks 1 and 2 are read by four dequant warps each, blocks 0 and 3 (all four
+      // on the split path) by the eight softmax warps
+      mbar_init(bar(c, B_OFREE + i), (P.n_splits == 1 && (i == 1 || i == 2)) ? 128 : N_SX);
     }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(bar(c, B_SFULL + i), 1);
-      mbar_init(bar(c, B_SFREE + i), N_SM);
+      mbar_init(bar(c, B_SFREE + i), N_SX);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(c, B_KRFULL + i), N_SM);
+      mbar_init(bar(c, B_KRFULL + i), N_SX);
       mbar_init(bar(c, B_KRFREE + i), 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(bar(c, B_ITFULL + i), N_PREP);
-      mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SM + N_EPI + 1);
+      mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SX + 1);
       mbar_init(bar(c, B_QSTAT + i), N_DQ);
     }
     mbar_init(bar(c, B_ODONE), 1);
     for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_DQ);
     mbar_init(bar(c, B_QFREE), 1);
-    mbar_init(bar(c, B_MFIN), N_SM);
-    mbar_init(bar(c, B_LREADY), N_EPI);
-    mbar_init(bar(c, B_SMG), N_SM);
-    mbar_init(bar(c, B_EPG), N_EPI);
+    mbar_init(bar(c, B_LREADY), N_SX);
+    mbar_init(bar(c, B_SXG), 128);
+    mbar_init(bar(c, B_SXG + 1), 128);
+    mbar_init(bar(c, B_SXA), N_SX);
     mbar_init(bar(c, B_DRAIN), 1);
     mbar_init(bar(c, B_NEVER), 1);   // nothing arrives: the failure-path test waits on it
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1370,12 +1341,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   // order are visible after this; a no-op for a launch without that dependency
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  if (warp < W_SM) {
+  if (warp < W_SX) {
     dq_role(P, c, tmem, warp, lane);
-  } else if (warp < W_EPI) {
-    sm_role(P, c, tmem, warp - W_SM, lane);
   } else if (warp < W_MMA) {
-    epi_role(P, c, tmem, warp - W_EPI, lane);
+    sx_role(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
   } else if (warp == W_MMA) {
     if (lane == 0) mma_role(P, c, tmem);
   } else if (warp == W_PREP) {
