@@ -782,89 +782,102 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
 }
 
 // ================================================================== MMA issuer
-// Descriptor plus a byte offset: the start address field holds address >> 4 in the low
-// 14 bits, and no offset used here carries out of it.
-// (an asm add, so that the compiler does not hoist every descriptor of the unrolled loops
-// into registers)
-DSA_DEV uint64_t dadd(uint64_t d, uint32_t bytes) {
-  uint32_t lo;
-  asm volatile("add.u32 %0, %1, %2;" : "=r"(lo) : "r"((uint32_t)d), "r"(bytes >> 4));
-  return ((uint64_t)(uint32_t)(d >> 32) << 32) | lo;
+// The whole warp runs this role and one elected lane issues each tensor-core
+// instruction: with warp-uniform control flow the descriptor arithmetic stays in uniform
+// registers.  (Issued from one lane of a divergent branch, every MMA paid conversions
+// into uniform registers: 130-160 cycles per M = 128, N = 64, K = 16 MMA against the 48
+// its operands take.)
+DSA_DEV bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
+DSA_DEV void issue_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  if (elect_one()) mma_ss(d, adesc, bdesc, idesc, acc);
+  __syncwarp();
+}
+DSA_DEV void issue_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  if (elect_one()) mma_ts(d, a, bdesc, idesc, acc);
+  __syncwarp();
+}
+DSA_DEV void commit(uint32_t bar_addr) {
+  if (elect_one()) tc_commit(bar_addr);
+  __syncwarp();
 }
 
 DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   constexpr uint32_t IDESC_QK = idesc_f16(128, NQ, 0, 0);
   constexpr uint32_t IDESC_PV = idesc_f16(128, NQ, 1, 1);
-  // every descriptor of the loop is one of these plus a constant offset
+  // every descriptor of the loop is one of these plus a constant offset (in 16-byte units
+  // in the low 14-bit address field; no offset used here carries out of it)
   const uint64_t d_k = sdesc(c.sb + SM_V, 16, 1024);        // codes tile, K-major (QK^T)
   const uint64_t d_v = sdesc(c.sb + SM_V, 16384, 1024);     // codes tile, MN-major (PV)
   const uint64_t d_q = sdesc(c.sb + SM_Q, 16, 1024);        // q~ hi / lo
   uint32_t g = 0, nq = 0, np = 0;
   for (uint32_t seq = 0;; ++seq) {
     const int b = seq % NB;
-    if (!wait_bar(c, B_ITFULL + b, (seq / NB) & 1)) return;
+    if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return;
     const int* info = item_info(c, b);
     const int item = info[IT_ITEM];
     const int T = info[IT_T];
-    mbar_arrive(bar(c, B_ITEMPTY + b));
+    if (elect_one()) mbar_arrive(bar(c, B_ITEMPTY + b));
+    __syncwarp();
     if (item < 0) return;
     if (T == 0) continue;
     for (int tt = 0; tt < T; ++tt) {
       // ---- partial scores T_p = codes_p . q~_p^T, one per latent chunk, then the rope part
-      // (chunk loop not unrolled: a smaller issue loop misses the instruction caches less,
-      // which the one issuing thread would otherwise stall on)
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
         const int cidx = qk_chunk(p);
         const uint32_t sbf = np % NSB;
-        if (!wait_bar(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
-        if (tt == 0 && !wait_bar(c, B_QRDY + cidx, nq & 1)) return;
-        if (!wait_bar(c, B_VFULL + cidx, g & 1)) return;
+        if (!wait_bar_w(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
+        if (tt == 0 && !wait_bar_w(c, B_QRDY + cidx, nq & 1)) return;
+        if (!wait_bar_w(c, B_VFULL + cidx, g & 1)) return;
         tc_fence_after();
         const uint32_t d_s = tmem + TM_S + 64 * sbf;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
           const uint32_t boff = (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
-          mma_ss(d_s, dadd(d_k, aoff), dadd(d_q, boff), IDESC_QK, kk ? 1u : 0u);
+          issue_ss(d_s, d_k + (aoff >> 4), d_q + (boff >> 4), IDESC_QK, kk ? 1u : 0u);
         }
-        tc_commit(bar(c, B_SFULL + sbf));
+        commit(bar(c, B_SFULL + sbf));
         ++np;
       }
       {
         const uint32_t sbf = np % NSB;
         const uint32_t kb = g & 1;
-        if (!wait_bar(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
-        if (tt == 0 && !wait_bar(c, B_QRDY + 4, nq & 1)) return;
-        if (!wait_bar(c, B_KRFULL + kb, (g >> 1) & 1)) return;
+        if (!wait_bar_w(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
+        if (tt == 0 && !wait_bar_w(c, B_QRDY + 4, nq & 1)) return;
+        if (!wait_bar_w(c, B_KRFULL + kb, (g >> 1) & 1)) return;
         tc_fence_after();
         const uint32_t d_s = tmem + TM_S + 64 * sbf;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(d_s, tmem + TM_KR + 32 * kb + 8 * kk, dadd(d_q, 8 * 8192 + kk * 32), IDESC_QK, kk ? 1u : 0u);
-        tc_commit(bar(c, B_SFULL + sbf));
-        tc_commit(bar(c, B_KRFREE + kb));
+          issue_ts(d_s, tmem + TM_KR + 32 * kb + 8 * kk, d_q + ((8 * 8192 + kk * 32) >> 4), IDESC_QK, kk ? 1u : 0u);
+        commit(bar(c, B_SFULL + sbf));
+        commit(bar(c, B_KRFREE + kb));
         ++np;
       }
-      if (tt == T - 1) tc_commit(bar(c, B_QFREE));   // q~ may be rebuilt after these MMAs
+      if (tt == T - 1) commit(bar(c, B_QFREE));   // q~ may be rebuilt after these MMAs
       // ---- O^T_b += codes_b^T . P_b, one block of output dims per latent block
 #pragma unroll 1
       for (int pb = 0; pb < 4; ++pb) {
-        if (!wait_bar(c, B_PFULL + pb, g & 1)) return;
+        if (!wait_bar_w(c, B_PFULL + pb, g & 1)) return;
         tc_fence_after();
         if (tt == 0 && nq > 0) {
           // the previous item's epilogue has read this part of O^T
-          if (!wait_bar(c, B_OFREE + pb, (nq - 1) & 1)) return;
+          if (!wait_bar_w(c, B_OFREE + pb, (nq - 1) & 1)) return;
           tc_fence_after();
         }
         const uint64_t d_p = sdesc(c.sb + p_buffer(pb), 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + TM_O + 64 * pb, dadd(d_v, pb * 32768 + kk * 2048), dadd(d_p, kk * 2048), IDESC_PV,
-                 (tt > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(c, B_PVD + pb));
+          issue_ss(tmem + TM_O + 64 * pb, d_v + ((pb * 32768 + kk * 2048) >> 4), d_p + ((kk * 2048) >> 4), IDESC_PV,
+                   (tt > 0 || kk > 0) ? 1u : 0u);
+        commit(bar(c, B_PVD + pb));
       }
-      if (tt == T - 1) tc_commit(bar(c, B_ODONE));
+      if (tt == T - 1) commit(bar(c, B_ODONE));
       ++g;
     }
     ++nq;
@@ -1346,7 +1359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   } else if (warp < W_MMA) {
     sx_role(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
   } else if (warp == W_MMA) {
-    if (lane == 0) mma_role(P, c, tmem);
+    mma_role(P, c, tmem);
   } else if (warp == W_PREP) {
     prep_role(P, c, lane);
   }
