@@ -41,9 +41,9 @@
 //
 // TMEM: O^T 0..255 (4 blocks x [32 hi | 32 lo]), partial scores 256..447 (three
 // buffers), rope keys 448..511 (two).  Shared memory: q~ 72 KB, codes tile 128 KB, one
-// 16 KB P buffer.  P_1 and P_3 borrow the first halves of code chunks 0 and 1 once PV
-// of blocks 0 and 1 has read them, so the next tile's QK^T takes its chunks in the
-// order 0, 2, 1, 3, the order in which they come free.
+// 16 KB P buffer.  P_1 and P_2 borrow code chunk 0 once PV of block 0 has read it, so
+// the next tile's QK^T takes its chunks in the order 1, 0, 2, 3, the order in which they
+// come free.
 // With few tokens each token's rows are split over several CTAs, one item per CTA, and
 // the launch is cooperative: once its roles are done, every split of a (token, half)
 // waits for the others and combines its share of the fp32 partial outputs.
@@ -118,10 +118,14 @@ enum { IT_ITEM = 0, IT_TOKEN, IT_HALF, IT_SPLIT, IT_T, IT_ROW0, IT_NROWS, IT_REF
 
 // The QK^T order of the latent chunks (p-th partial -> chunk), the PV event after which
 // chunk c of the codes tile may be overwritten by the next tile, and where P_b lives.
-DSA_DEV int qk_chunk(int p) { return p == 1 ? 2 : (p == 2 ? 1 : p); }
-DSA_DEV int chunk_free_event(int c) { return c == 0 ? 1 : (c == 2 ? 2 : 3); }
+// P_0 goes into the shared P buffer; once PV(0) has completed, chunk 0 (two 16 KB halves)
+// and the shared buffer take P_1, P_2 and P_3 together, so one handoff per tile gates PV.
+// Chunk 1 is then free first (after PV(1)), chunks 0 and 2 after PV(2), chunk 3 after
+// PV(3): the next tile's QK^T takes them in the order 1, 0, 2, 3.
+DSA_DEV int qk_chunk(int p) { return p == 0 ? 1 : (p == 1 ? 0 : p); }
+DSA_DEV int chunk_free_event(int c) { return c == 1 ? 1 : (c == 3 ? 3 : 2); }
 DSA_DEV uint32_t p_buffer(int b) {
-  return b == 1 ? SM_V : (b == 3 ? SM_V + 32768u : SM_P);
+  return b == 1 ? SM_V : (b == 2 ? SM_V + 16384u : SM_P);
 }
 
 struct KParams {
@@ -628,7 +632,7 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
 // k = 0..3, per 128-dim chunk: eight lanes read 128 contiguous bytes of a row.  The
 // fp16 codes go straight into the 128-byte-swizzled tile (rows of 128 bytes holding 64
 // dims); the four rows of one store instruction alternate in row parity, which keeps the
-// stores free of bank conflicts.  Chunks are converted in the QK^T order (0, 2, 1, 3);
+// stores free of bank conflicts.  Chunks are converted in the QK^T order (1, 0, 2, 3);
 // raw bytes are loaded two chunks ahead of their conversion (position p of a tile lives
 // in register slot p % 2).
 // An entry for a row past the end of the item: no list entry has every bit set, since
@@ -1098,14 +1102,12 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         }
         tc_wait_st();
       }
-      // ---- P_b hi / lo for the four PV blocks, each as soon as its buffer is free: P_0 in
-      // the shared buffer (last read by PV(2) of the previous tile), P_1 / P_2 after PV(0)
-      // of this tile (chunk 0, the shared buffer), P_3 after PV(1) (chunk 1).  The row
-      // sums go between P_0 and P_1.
+      // ---- P_b hi / lo for the four PV blocks: P_0 in the shared buffer (last read by
+      // PV(3) of the previous tile), P_1 .. P_3 once PV(0) of this tile has completed
+      // (chunk 0 and the shared buffer).  The row sums go between P_0 and P_1.
 #pragma unroll 1
       for (int pb = 0; pb < 4; ++pb) {
-        const int ev = pb == 0 ? 2 : (pb == 3 ? 1 : 0);
-        if (!wait_bar_w(c, B_PVD + ev, pb == 0 ? ((g & 1) ^ 1) : (g & 1))) return;
+        if (pb < 2 && !wait_bar_w(c, B_PVD + (pb == 0 ? 3 : 0), pb == 0 ? ((g & 1) ^ 1) : (g & 1))) return;
         const float f = (pb == 0 ? sc[0] : pb == 1 ? sc[1] : pb == 2 ? sc[2] : sc[3]) * iref[pb];
         store_pb(c.sb + p_buffer(pb), r, gq, y, valid ? f : 0.f);
         fence_async_smem();
