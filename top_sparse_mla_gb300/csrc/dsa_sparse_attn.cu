@@ -71,6 +71,7 @@ constexpr int W_SX = 8, W_MMA = 16, W_PREP = 17;
 constexpr int NWARPS = 18;
 constexpr int NTHREADS = 32 * NWARPS;
 constexpr int N_DQ = 256, N_SX = 256, N_PREP = 32;
+constexpr int WG_DQ = N_DQ / 32, WG_SX = N_SX / 32;   // warps: the unit of the handoff barriers' counts
 constexpr int MAX_SPLITS = 16;
 constexpr int NB = 4;              // item buffers: the prep warp runs up to NB - 1 items ahead
 constexpr int NSB = 3;             // partial-score buffers in TMEM
@@ -171,6 +172,13 @@ struct Ctx {
 constexpr unsigned long long WAIT_LIMIT_CYCLES = 4000000000ull;   // ~2 s at 2 GHz
 
 DSA_DEV uint32_t bar(const Ctx& c, int i) { return c.sb + SM_BAR + 8u * (uint32_t)i; }
+// Arrival of a whole warp as one: after the warp's lanes meet (which orders their memory
+// operations), lane 0 arrives.  Barriers that warps signal this way count warps, not
+// threads, so a 256-thread handoff costs 8 arrive operations instead of 256.
+DSA_DEV void arrive_w(const Ctx& c, int b) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar(c, b));
+}
 
 // The waiting part of a bounded wait, out of line: one copy serves every wait site (the
 // code of all roles shares the SM's instruction caches).  False when the limit passes
@@ -206,7 +214,7 @@ struct Group {
   int b;
   uint32_t n;
   DSA_DEV bool sync(const Ctx& c) {
-    mbar_arrive(bar(c, b));
+    arrive_w(c, b);
     const bool ok = wait_bar_w(c, b, n & 1);
     ++n;
     return ok;
@@ -347,7 +355,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     }
     if (item < 0) {
       if (lane == 0) info[IT_ITEM] = -1;
-      mbar_arrive(bar(c, B_ITFULL + b));   // tells every role to stop
+      arrive_w(c, B_ITFULL + b);   // tells every role to stop
       return;
     }
     const int row0 = tile0 * TILE;
@@ -392,7 +400,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       info[IT_REF + lane] = (int)(ebits[lane] << 23);            // 2^(e - 127)
       info[IT_IREF + lane] = (int)((254u - ebits[lane]) << 23);  // 2^(127 - e)
     }
-    mbar_arrive(bar(c, B_ITFULL + b));   // rows, tile range, reference scales, rotary table
+    arrive_w(c, B_ITFULL + b);   // rows, tile range, reference scales, rotary table
   }
 }
 
@@ -519,7 +527,7 @@ __device__ __noinline__ void epi_chunk(const Ctx& c, uint32_t tmem, int q4, int 
     }
     if (hg == ng - 1) {
       tc_fence_before();
-      mbar_arrive(bar(c, B_OFREE + cidx));   // this share of O^T has been read
+      arrive_w(c, B_OFREE + cidx);   // this share of O^T has been read
     }
     if (part) {
       float* o = part + (size_t)col * D_LAT + d;
@@ -618,13 +626,13 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
     if ((a & 1) == 1 || a == 8) {
       // latent chunk a / 2 (atoms a - 1, a) or the rotary atom is complete
       fence_async_smem();
-      mbar_arrive(bar(c, B_QRDY + (a >> 1)));
+      arrive_w(c, B_QRDY + (a >> 1));
     }
   }
   float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 32 * b;
   if (chn == 0) s_inv[hs] = hv ? rsqrtf(ss * (1.0f / D_QK) + P.eps) * P.c2 * __uint_as_float((uint32_t)(127 - k) << 23)
                                : 0.f;
-  mbar_arrive(bar(c, B_QSTAT + b));
+  arrive_w(c, B_QSTAT + b);
 }
 
 // ================================================================== DQ
@@ -683,7 +691,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
     const int cidx = 1 + (w >> 2);
     epi_chunk<8>(c, tmem, w & 3, lane, cidx, 0, HH / 8, reinterpret_cast<const float*>(c.sm + SM_EL),
                  item_ref(c, pbf)[cidx], O, pinfo[IT_TOKEN], HH * pinfo[IT_HALF], nullptr, rope);
-    mbar_arrive(bar(c, B_ITEMPTY + pbf));
+    arrive_w(c, B_ITEMPTY + pbf);
     pend = -1;
     return true;
   };
@@ -704,8 +712,8 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
         dq_load_chunk(P, raw[1], qk_chunk(1), cur, ch);
         return 1;
       }
-      mbar_arrive(bar(c, B_QSTAT + b));   // no q~: the phase still follows the buffer's uses
-      mbar_arrive(bar(c, B_ITEMPTY + b));
+      arrive_w(c, B_QSTAT + b);   // no q~: the phase still follows the buffer's uses
+      arrive_w(c, B_ITEMPTY + b);
       ++seq;
     }
   };
@@ -754,7 +762,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
           sts128(rb + ((pb ^ rsw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
         }
         fence_async_smem();
-        mbar_arrive(bar(c, B_VFULL + cidx));
+        arrive_w(c, B_VFULL + cidx);
         if (pos == 0 && pf && ch < 6) {
           // the six 128-byte lines of each next row, one line per lane
 #pragma unroll
@@ -776,7 +784,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       pend = (int)seq;
       pend_nq = nq;
     } else {
-      mbar_arrive(bar(c, B_ITEMPTY + b));
+      arrive_w(c, B_ITEMPTY + b);
     }
     ++nq;
     ++seq;
@@ -920,7 +928,7 @@ DSA_DEV void sx_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tla
   tmem_st16(tmem + tlane + TM_KR + 32 * kb + 16 * gq, v);
   tc_wait_st();
   tc_fence_before();
-  mbar_arrive(bar(c, B_KRFULL + kb));
+  arrive_w(c, B_KRFULL + kb);
 }
 
 // P_b = P * scale_b / reference_b of row r for the group's 16 heads, as hi / lo fp16 into
@@ -990,7 +998,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         if (r < 16) P.part_lse[((size_t)t * P.n_splits + split) * 64 + HH * half + hb + r] = -INFINITY;
         if (!count_in(t, split, half)) return -1;
       }
-      mbar_arrive(bar(c, B_ITEMPTY + b));
+      arrive_w(c, B_ITEMPTY + b);
       ++seq;
     }
   };
@@ -1044,7 +1052,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         tmem_ld16(ts + HH, l);
         tc_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(c, B_SFREE + sbf));
+        arrive_w(c, B_SFREE + sbf);
 #pragma unroll
         for (int i = 0; i < 16; ++i) y[i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[i]);
         ++np;
@@ -1112,7 +1120,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         store_pb(c.sb + p_buffer(pb), r, gq, y, valid ? f : 0.f);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(c, B_PFULL + pb));
+        arrive_w(c, B_PFULL + pb);
         if (pb == 0) {
           // this warp's row sums (lanes 2m, 2m + 1: head hb + m)
           float v[16];
@@ -1147,7 +1155,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       }
       // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
       // is out
-      if (!is_split) mbar_arrive(bar(c, B_LREADY));
+      if (!is_split) arrive_w(c, B_LREADY);
       const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
       float* part = is_split ? P.part_o + (((size_t)t * P.n_splits + split) * 64 + h0) * D_LAT : nullptr;
@@ -1160,7 +1168,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       }
       if (is_split && !count_in(t, split, half)) return;
     }
-    mbar_arrive(bar(c, B_ITEMPTY + b));
+    arrive_w(c, B_ITEMPTY + b);
     ++seq;
     ++nq;
     if (open_item() <= 0) return;
@@ -1314,33 +1322,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(c, B_VFULL + i), N_DQ);
+      mbar_init(bar(c, B_VFULL + i), WG_DQ);
       mbar_init(bar(c, B_PVD + i), 1);
-      mbar_init(bar(c, B_PFULL + i), N_SX);
+      mbar_init(bar(c, B_PFULL + i), WG_SX);
       // O^T blocks 1 and 2 are read by four dequant warps each, blocks 0 and 3 (all four
-      // on the split path) by the eight softmax warps
-      mbar_init(bar(c, B_OFREE + i), (P.n_splits == 1 && (i == 1 || i == 2)) ? 128 : N_SX);
+      // on the split path) by the eight softmax warps (counts in warps)
+      mbar_init(bar(c, B_OFREE + i), (P.n_splits == 1 && (i == 1 || i == 2)) ? 4 : WG_SX);
     }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(bar(c, B_SFULL + i), 1);
-      mbar_init(bar(c, B_SFREE + i), N_SX);
+      mbar_init(bar(c, B_SFREE + i), WG_SX);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(c, B_KRFULL + i), N_SX);
+      mbar_init(bar(c, B_KRFULL + i), WG_SX);
       mbar_init(bar(c, B_KRFREE + i), 1);
     }
     for (int i = 0; i < NB; ++i) {
-      mbar_init(bar(c, B_ITFULL + i), N_PREP);
-      mbar_init(bar(c, B_ITEMPTY + i), N_DQ + N_SX + 1);
-      mbar_init(bar(c, B_QSTAT + i), N_DQ);
+      mbar_init(bar(c, B_ITFULL + i), 1);
+      mbar_init(bar(c, B_ITEMPTY + i), WG_DQ + WG_SX + 1);
+      mbar_init(bar(c, B_QSTAT + i), WG_DQ);
     }
     mbar_init(bar(c, B_ODONE), 1);
-    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), N_DQ);
+    for (int i = 0; i < 5; ++i) mbar_init(bar(c, B_QRDY + i), WG_DQ);
     mbar_init(bar(c, B_QFREE), 1);
-    mbar_init(bar(c, B_LREADY), N_SX);
-    mbar_init(bar(c, B_SXG), 128);
-    mbar_init(bar(c, B_SXG + 1), 128);
-    mbar_init(bar(c, B_SXA), N_SX);
+    mbar_init(bar(c, B_LREADY), WG_SX);
+    mbar_init(bar(c, B_SXG), 4);
+    mbar_init(bar(c, B_SXG + 1), 4);
+    mbar_init(bar(c, B_SXA), WG_SX);
     mbar_init(bar(c, B_DRAIN), 1);
     mbar_init(bar(c, B_NEVER), 1);   // nothing arrives: the failure-path test waits on it
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
