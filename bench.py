@@ -8,9 +8,11 @@ lengths, NaN-filled stale rows); the line also carries the other workload sizes.
 Timing: W untimed warm-up steps, then K steps; L2 is flushed (a 512 MiB write) before
 every timed step, each step is timed with CUDA events on the launching stream, and
 the K-step region is bracketed by a barrier and a device synchronize.  With N > 1
-(torchrun) every rank runs its own copy of the workload on its own GPU (independent
-problems, no collective on the data path); the value is the tokens of all ranks over
-the slowest rank's time.
+(torchrun) the ranks split one batch: rank r takes a contiguous slice of the workload's
+tokens (query tokens are independent problems, so there is no collective on the data
+path) and the value is the batch's tokens over the slowest rank's time (strong
+scaling).  --replicas instead gives every rank its own copy of the whole workload (weak
+scaling).
 
 --impl reference times the CPU oracle (float64 numpy, test infrastructure) on
 bounded samples of the same workload; only rank 0 runs it.
@@ -38,6 +40,15 @@ HEADLINE = "decode1024"
 METRIC = "sparse-attn tokens/s and us/call, s_q=1..2123; HBM GB/s and % of roofline"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+# the roofline the workload specification defines: the larger of the gathered bytes at
+# 8 TB/s and the flops at the dense peak of the MMA precision used (fp16 operands, fp32
+# accumulate: 2.25 PFLOP/s nominal on GB300)
+SPEC_HBM_BPS = 8e12
+SPEC_DENSE_FLOPS = 2.25e15
+
+
+def spec_roofline_s(w) -> float:
+    return max(algorithmic_bytes(w) / SPEC_HBM_BPS, algorithmic_flops(w) / SPEC_DENSE_FLOPS)
 
 
 def algorithmic_bytes(w) -> int:
@@ -137,6 +148,15 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def rank_workload(w, rank: int, world: int, replicas: bool = False):
+    """The part of the batch this rank runs: its contiguous token slice of `w` (the caches
+    are shared), or all of `w` in replica mode."""
+    if world > 1 and not replicas:
+        from top_sparse_mla_gb300 import sharding
+        return sharding.shard(w, rank, world)
+    return w
 
 
 def dist_setup(n_gpus: int):
@@ -290,7 +310,8 @@ def run_native(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     peak, peak_kind = measured_peaks()
 
-    w = W.make(args.workload)
+    w_full = W.make(args.workload)
+    w = rank_workload(w_full, rank, world, args.replicas)
     inp = api.upload(w, "cuda")
     out = api.allocate_outputs(inp)
     sampler = ClockSampler(local)
@@ -308,7 +329,7 @@ def run_native(args):
     clocks = sampler.stop()
     ms = statistics.mean(times)
     ms_max = max_over_ranks(pg, ms)
-    tokens_total = w.s_q * world
+    tokens_total = w_full.s_q * (world if args.replicas else 1)
     value = tokens_total / (ms_max * 1e-3)
     b_alg = algorithmic_bytes(w)
     achieved = b_alg / (ms * 1e-3) / 1e9
@@ -321,7 +342,7 @@ def run_native(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     per_config = {}
-    if not args.skip_sweep:
+    if not args.skip_sweep and world == 1:
         for name in ("decode1", "decode64", "decode1024", "prefill2123"):
             wc = W.make(name) if name != args.workload else w
             ic = api.upload(wc, "cuda") if name != args.workload else inp
@@ -333,6 +354,8 @@ def run_native(args):
                                 "tokens_per_s": wc.s_q / (med * 1e-3), "alg_bytes": bc,
                                 "alg_gbs": bc / (med * 1e-3) / 1e9, "frac_of_hbm_peak": bc / (med * 1e-3) / 1e9 / peak,
                                 "alg_tflops": algorithmic_flops(wc) / (med * 1e-3) / 1e12,
+                                "spec_roofline_us": spec_roofline_s(wc) * 1e6,
+                                "frac_of_spec_roofline": spec_roofline_s(wc) / (med * 1e-3),
                                 "n_valid_rows": int(W.n_valid_rows(wc).sum())}
             if name != args.workload:
                 del ic, oc
@@ -340,26 +363,33 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        rate, ntok, dt = cpu_oracle_rate(w)
+        rate, ntok, dt = cpu_oracle_rate(w_full)
         cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"first {ntok} tokens of {w.name} in {dt:.1f} s, numpy float64, BLAS default threads"}
+               "sample": f"first {ntok} tokens of {w_full.name} in {dt:.1f} s, numpy float64, BLAS default threads"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak" if (world == 1 or args.replicas) else "strong",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": w.name, "s_q": w.s_q, "h_q": w.h_q, "topk": w.topk,
-                       "n_valid_rows": int(W.n_valid_rows(w).sum()), "parallelism": f"independent x{world}",
+            "config": {"workload": w_full.name, "s_q": w_full.s_q, "h_q": w.h_q, "topk": w.topk,
+                       "n_valid_rows": int(W.n_valid_rows(w_full).sum()),
+                       "parallelism": (f"replicas x{world}" if args.replicas else f"token slices x{world}") if world > 1
+                       else "single GPU",
                        "l2": "flushed before every timed step (512 MiB write)",
-                       "operands": "fp8 e4m3 cache dequantised to fp16, fp32 accumulate, MXFP8 out",
+                       "operands": "E4M3 codes exact in fp16, fp32 block scales applied in fp32, q~ and P as "
+                                   "fp16 hi + lo pairs, fp32 accumulate, MXFP8 out",
                        "timed_wall_s": wall},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": args.traffic if args.traffic is not None else profiled_traffic(args.workload),
                          "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
                                            "(profiles/dsa_fwd_kernel_decode1024_full.md)",
                          "peak_source": peak_kind,
-                         "alg_bytes_per_launch": b_alg},
+                         "alg_bytes_per_launch": b_alg,
+                         "spec_roofline_us": spec_roofline_s(w) * 1e6,
+                         "frac_of_spec_roofline": spec_roofline_s(w) / (ms * 1e-3),
+                         "spec_roofline_definition": "max(alg bytes / 8 TB/s, alg flops / 2.25 PFLOP/s fp16 dense)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps * kernels_per_call(inp.params),
@@ -380,6 +410,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end timing")
     ap.add_argument("--no-soak", action="store_true", help="no clock-sampling soak after the timed steps")
     ap.add_argument("--skip-cpu", action="store_true", help="no CPU oracle baseline")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with N > 1: every rank runs the whole workload (weak scaling) instead of a token slice")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the kernel from an ncu capture, if known")
     args = ap.parse_args()

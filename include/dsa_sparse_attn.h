@@ -29,12 +29,22 @@
  *   indices     int32 [s_q, topk]   (-1 or any negative value = skip)
  *   topk_length int32 [s_q]         (values <= 0 read nothing; values > topk read topk)
  *   positions   int32 [s_q]
- *   norm_w      bf16  [576]
+ *   norm_w      bf16  [576]                              16-byte aligned
  *   out_fp8     uint8 [s_q, h_q, 512] E4M3 codes          16-byte aligned
  *   out_sf      uint8 [s_q, h_q, 16]  UE8M0 codes
  *   out_precast fp32  [s_q, h_q, 512] (debug entry only; may be NULL) 16-byte aligned
  *   lse         fp32  [s_q, h_q] natural-log sum-exp of the scaled scores, -inf for
  *               a token with no valid column (debug entry only; may be NULL)
+ *
+ * Numerics: the contractions run on fp16 tensor-core MMAs with fp32 accumulation, and
+ * every operand is exact in fp16 or split into an exact-enough fp16 hi + lo pair: the
+ * E4M3 codes are exact in fp16 and the rows' fp32 block scales are applied in fp32 per
+ * 128-value block; q * norm_w (exact in fp32) goes in as hi + lo with a per-head
+ * power-of-two prescale; the softmax weights times each block's scales go in as hi + lo.
+ * The pre-cast output then agrees with a float64 evaluation to about 1e-6 relative, for
+ * any scaling of q, norm_w or a row's block scales.  Ranges: a rope key (bf16) must be
+ * below 65504 in magnitude (it is converted to fp16); the E4M3 NaN code is not expected
+ * in a referenced row.
  *
  * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream),
  * allocate nothing, and enqueue two operations: a small memset or a one-CTA ordering
@@ -112,9 +122,10 @@ int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32
 size_t dsa_sparse_attn_workspace_size(const dsa_params* p, int num_sms);
 
 /* The fused forward pass (steps 1-7), enqueued on `stream`; everything it enqueues can
- * be captured in a CUDA graph.
+ * be captured in a CUDA graph.  A work item is one token's heads 0..31 or 32..63 (one
+ * item per token when h_q <= 32), or a KV split of that.
  * - When the tokens are few (dsa_sparse_attn_num_splits > 1), each CTA takes one
- *   (token, split) item. The call clears the workspace header and the combine counters
+ *   (token, heads, split) item. The call clears the workspace header and the combine counters
  *   with an async memset. The fused kernel's launch is then cooperative, so that the
  *   splits of a token can wait for one another before each combines its share of the
  *   partial outputs; the grid is at most one CTA per SM.
@@ -156,10 +167,17 @@ int dsa_sparse_attn_read_status(const void* workspace, uint32_t* status, void* s
  *   - The first call on each device (that device current) looks up the scratch
  *     address with cudaGetSymbolAddress; make that first call before any stream
  *     capture.
+ *   - Loading the library reserves the scratch on every device where the module is
+ *     loaded, whichever entry point the caller uses.
  *   - The scratch covers every shape whose workspace (dsa_sparse_attn_workspace_size)
  *     is at most DSA_NOALLOC_SCRATCH_BYTES: on a 152-SM GB300 any shape with
- *     s_q <= 5000000.  Larger shapes return DSA_ERR_SCRATCH_LIMIT with nothing
- *     enqueued.
+ *     s_q <= 2500000 (5000000 with h_q <= 32).  The workspace holds 4 bytes per token
+ *     and head half, 32 KB of row lists per SM
+ *     and, on the split path, 128 KB of fp32 partial output per (token, split); the
+ *     split path runs at most one item per SM, so its partials stay below
+ *     SMs x 128 KB (about 24.9 MB in all on 152 SMs, inside the scratch; a part with
+ *     more SMs could exceed it).  Larger shapes return DSA_ERR_SCRATCH_LIMIT with
+ *     nothing enqueued.
  *   - The scratch header is cleared on `stream` before each launch.
  *   - All calls on one device share the one scratch array: calls that overlap on the
  *     GPU (different streams, not ordered by events) race and give undefined results.

@@ -25,7 +25,7 @@
  * It allocates nothing, launches one kernel with one CTA per row, and can be captured
  * in a CUDA graph. It returns DSA_OK, or one of the following with nothing enqueued:
  *   - DSA_ERR_INVALID_ARG: a bad size, a null or misaligned pointer;
- *   - DSA_ERR_UNSUPPORTED_DEVICE: not compute capability 10.3;
+ *   - DSA_ERR_UNSUPPORTED_DEVICE: not compute capability 10.3, or a device ordinal >= DSA_MAX_DEVICES;
  *   - DSA_ERR_CUDA.
  */
 #ifndef DSA_TOPK_H_

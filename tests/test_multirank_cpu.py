@@ -1,5 +1,7 @@
 """World-size-2 checks of the multi-rank path on CPU (gloo): token sharding covers the
-batch exactly once, sharded results reassemble to the unsharded ones, and the
+batch exactly once; each rank takes bench.py's slice of the batch and prepares the
+library call for it (parameters, split count, workspace size, launches) through the C
+ABI's host entry points; sharded results reassemble to the unsharded ones; and the
 max-over-ranks timing reduction bench.py uses returns the slowest rank."""
 
 import os
@@ -28,10 +30,20 @@ def _worker(rank, world, port, out_dir):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import oracle
     import bench
-    from top_sparse_mla_gb300 import sharding, workloads as W
+    from top_sparse_mla_gb300 import native, sharding, workloads as W
     w = W.random_case(77, s_q=7, h_q=4, n_swa_cols=16, n_cmp_cols=48, n_swa_rows=128, n_cmp_rows=256,
                       n_sentinels=4, lengths="ragged")
-    part = sharding.shard(w, rank, world)
+    part = bench.rank_workload(w, rank, world)
+    assert bench.rank_workload(w, rank, world, replicas=True) is w
+    # the library call this rank would make for its slice (host entry points only)
+    native.library()
+    p = native.dsa_params_init(part.s_q, part.h_q, part.topk, part.n_swa_cols, part.kv_swa.shape[0],
+                               part.kv_cmp.shape[0])
+    ns = native.dsa_sparse_attn_num_splits(p, 152)
+    ws = native.dsa_sparse_attn_workspace_size(p, 152)
+    assert ns >= 1 and ws >= 256 and ws % 256 == 0
+    assert bench.kernels_per_call(p, 152) == (2 if ns == 1 else 1)
+    dist.all_gather_object(info := [None] * world, (part.s_q, ns, ws))
     r = oracle.sparse_mla_forward(part.q, part.kv_swa, part.kv_cmp, part.indices, part.topk_length,
                                   part.positions, part.norm_w, oracle.OracleParams(n_swa_cols=w.n_swa_cols))
     # variable-size shards: pad to the largest, gather, trim
@@ -42,6 +54,7 @@ def _worker(rank, world, port, out_dir):
     gathered = [torch.zeros_like(buf) for _ in range(world)]
     dist.all_gather(gathered, buf)
     slowest = bench.max_over_ranks(dist, float(rank + 1) * 0.25)
+    assert sum(x[0] for x in info) == w.s_q
     if rank == 0:
         pieces = []
         for k in range(world):

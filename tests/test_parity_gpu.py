@@ -132,3 +132,36 @@ def test_deterministic_and_production_entry_matches_debug_entry():
     c = parity.run_gpu(w, debug=True)
     assert np.array_equal(a["out_fp8"], b["out_fp8"]) and np.array_equal(a["out_sf"], b["out_sf"])
     assert np.array_equal(a["out"], c["out"])
+
+
+def _scale_bf16(bits: np.ndarray, k: int) -> np.ndarray:
+    """bf16 bit patterns times 2^k (exact: the exponent field moves; zeros stay zero)."""
+    b = bits.astype(np.int32)
+    nz = (b & 0x7F80) != 0
+    return np.where(nz, b + (k << 7), b).astype(np.uint16)
+
+
+def _scale_latent(kv: np.ndarray, k: int) -> np.ndarray:
+    """fp8_ds_mla rows whose latent values are all times 2^k: the E4M3 codes stay, the four
+    fp32 block scales move (every 128-block amax moves with them)."""
+    out = kv.copy()
+    sc = np.ascontiguousarray(out[:, 512:528]).view("<f4").astype(np.float64)
+    out[:, 512:528] = np.ldexp(sc, k).astype("<f4").view(np.uint8)
+    return out
+
+
+@pytest.mark.parametrize("what,k", [("q", -12), ("q", 10), ("w", 4), ("latent", -8), ("latent", 8)])
+def test_input_range_scalings(what, k):
+    # The fp16 operands carry q * w with a per-head power-of-two prescale, and the cache's
+    # fp32 block scales stay in fp32: scaling q, the norm weight or a row's latent values
+    # by a power of two keeps the matching rule.
+    w = W.random_case(310 + k + 50 * len(what), s_q=5, h_q=64, n_swa_cols=128, n_cmp_cols=512, n_swa_rows=1024,
+                      n_cmp_rows=4096, n_sentinels=7, lengths="ragged")
+    if what == "q":
+        w.q = _scale_bf16(w.q, k)
+    elif what == "w":
+        w.norm_w = _scale_bf16(w.norm_w, k)
+    else:
+        w.kv_swa = _scale_latent(w.kv_swa, k)
+        w.kv_cmp = _scale_latent(w.kv_cmp, k)
+    _full(w)

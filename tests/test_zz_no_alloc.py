@@ -2,10 +2,13 @@
 entry point (dsa_sparse_attn_fwd), both through the C ABI.
 
 The two share the split choice and the kernel; the no-alloc call keeps its workspace in
-a scratch array built into the library.  Two calls in a row must both match, which
-shows that the second call starts from a cleared scratch header and clean combine
-counters.  This file is named so that pytest collects it last: it must pass on a
-process that has already run every other test, and on its own.
+a scratch array built into the library.  The kernel is deterministic (every output is
+computed by one fixed sequence of operations, whichever CTA takes it), so both calls of
+two in a row must reproduce the workspace entry point's codes and scales bit for bit:
+that shows the second call starts from a cleared scratch header and clean combine
+counters, which a looser comparison could hide.  This file is named so that pytest
+collects it last: it must pass on a process that has already run every other test, and
+on its own.
 """
 
 import ctypes
@@ -14,27 +17,13 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import codecs
 from top_sparse_mla_gb300 import api, native
 from top_sparse_mla_gb300 import workloads as W
 
-OUT_REL_L2 = 1e-2   # the pre-cast rule of the parity tests, applied to the dequantised codes
-
-
-def _dequant(fp8: np.ndarray, sf: np.ndarray) -> np.ndarray:
-    vals = codecs.e4m3_decode(fp8).reshape(fp8.shape[:-1] + (16, 32))
-    scale = np.exp2(sf.astype(np.float64) - 127.0)[..., None]
-    return (vals * scale).reshape(fp8.shape)
-
-
 def _assert_match(ref_fp8, ref_sf, fp8, sf, label):
     assert np.array_equal(sf, ref_sf), f"{label}: UE8M0 scale codes differ"
-    steps = codecs.e4m3_ulp_distance(fp8, ref_fp8)
-    assert int(steps.max(initial=0)) <= 1, f"{label}: E4M3 codes more than one step apart"
-    a, b = _dequant(fp8, sf), _dequant(ref_fp8, ref_sf)
-    denom = float(np.linalg.norm(b))
-    rel = float(np.linalg.norm(a - b) / denom) if denom > 0 else float(np.linalg.norm(a))
-    assert rel <= OUT_REL_L2, f"{label}: relative L2 difference {rel:.3e}"
+    diff = int((fp8 != ref_fp8).sum())
+    assert diff == 0, f"{label}: {diff} E4M3 codes differ from the workspace entry point's"
 
 
 def _outputs(inp):

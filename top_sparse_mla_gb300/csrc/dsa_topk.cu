@@ -15,6 +15,7 @@
 // output is ascending and the first `need` columns equal to T are the lowest-numbered.
 
 #include <cuda_runtime.h>
+#include <mutex>
 #include <stdint.h>
 
 #include "dsa_topk.h"
@@ -154,12 +155,19 @@ extern "C" int dsa_topk_select(const void* logits, int64_t ld, const int32_t* le
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED_DEVICE;
-  static int attr_done[64] = {0};
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(DSA_TOPK_MAX_COLS * sizeof(uint16_t))) != cudaSuccess)
-      return DSA_ERR_CUDA;
-    attr_done[dev] = 1;
+  if (dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
+  {
+    // the kernel's dynamic shared-memory limit, raised once per device (any host thread
+    // may make the first call)
+    static std::mutex attr_mutex;
+    static bool attr_done[DSA_MAX_DEVICES];
+    std::lock_guard<std::mutex> lock(attr_mutex);
+    if (!attr_done[dev]) {
+      if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(DSA_TOPK_MAX_COLS * sizeof(uint16_t))) != cudaSuccess)
+        return DSA_ERR_CUDA;
+      attr_done[dev] = true;
+    }
   }
   const size_t smem = (size_t)n * sizeof(uint16_t);
   topk_kernel<<<(unsigned)s_q, THREADS, smem, (cudaStream_t)stream>>>(
