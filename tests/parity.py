@@ -68,8 +68,13 @@ def near_power_of_two(amax: np.ndarray, rel: float = SF_BAND_REL) -> np.ndarray:
     return (amax > 0) & (np.abs(a / np.exp2(k) - 1.0) <= rel)
 
 
-def compare(gpu: dict, ref: dict, tokens=None, label: str = "") -> dict:
-    """Assert the matching rules; return (and record) the measured errors."""
+def compare(gpu: dict, ref: dict, tokens=None, label: str = "", out_scale: float = 1.0) -> dict:
+    """Assert the matching rules; return (and record) the measured errors.
+
+    out_scale: the factor by which the case scales the outputs relative to the
+    specification's value distributions (a power of two for the range cases): the
+    absolute pre-cast bound is stated for those distributions and scales with the data;
+    the relative and code-level rules do not change."""
     g_out, g_lse = gpu["out"], gpu["lse"]
     g_fp8, g_sf = gpu["out_fp8"], gpu["out_sf"]
     if tokens is not None:
@@ -102,7 +107,7 @@ def compare(gpu: dict, ref: dict, tokens=None, label: str = "") -> dict:
     summary = (f"{label}: fp8 within 1 step {frac:.6f} ({misses} of {n} misses), exact {exact:.6f}, "
                f"scale mismatches {int(sf_diff.sum())} ({sf_bad} outside the 1e-6 band), "
                f"max abs {max_abs:.3e}, rel L2 {rel_l2:.3e}, LSE {lse_err:.3e}")
-    assert max_abs <= OUT_MAX_ABS, f"pre-cast max abs error too large; {summary}"
+    assert max_abs <= OUT_MAX_ABS * out_scale, f"pre-cast max abs error too large; {summary}"
     assert rel_l2 <= OUT_REL_L2, f"pre-cast relative L2 error too large; {summary}"
     assert np.array_equal(inf_r, inf_g), f"-inf LSE pattern differs; {summary}"
     assert lse_err <= LSE_ABS, f"LSE error too large; {summary}"

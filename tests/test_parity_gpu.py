@@ -18,13 +18,13 @@ def _lib():
     native.library()
 
 
-def _full(w, **kw):
+def _full(w, out_scale=1.0, **kw):
     g = parity.run_gpu(w, **kw)
     # a bounded wait that ran out (or an index the kernel rejected) is reported as such,
     # before any value comparison
     assert g["status"] == 0 or kw.get("flags", 0), f"{w.name}: kernel status {g['status']:#x}"
     r = parity.run_oracle(w)
-    return g, r, parity.compare(g, r, label=w.name)
+    return g, r, parity.compare(g, r, label=w.name, out_scale=out_scale)
 
 
 def test_tiny_workload_all_elements():
@@ -164,4 +164,7 @@ def test_input_range_scalings(what, k):
     else:
         w.kv_swa = _scale_latent(w.kv_swa, k)
         w.kv_cmp = _scale_latent(w.kv_cmp, k)
-    _full(w)
+    w.name = f"range {what} x2^{k}"
+    # o is a weighted mean of the latent rows: it scales with them (q and w only sharpen
+    # or flatten the softmax)
+    _full(w, out_scale=2.0 ** k if what == "latent" and k > 0 else 1.0)
