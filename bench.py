@@ -247,6 +247,34 @@ def time_e2e(w, inp, out, steps: int, warmup: int, flush):
     return times, h2d, d2h
 
 
+def time_topk(s_q: int, n: int, k: int, flush, peak_gbs: float):
+    """The index producer's top-k selection (include/dsa_topk.h) on seeded N(0,1) bf16
+    logits: median CUDA-event time of 30 calls, L2 flushed before each; bytes are the
+    logits read plus the index rows and lengths written."""
+    import torch
+    from top_sparse_mla_gb300 import native
+    g = torch.Generator(device="cuda").manual_seed(7)
+    logits = torch.randn((s_q, n), generator=g, device="cuda").to(torch.bfloat16)
+    idx = torch.empty((s_q, k), dtype=torch.int32, device="cuda")
+    tl = torch.empty((s_q,), dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        native.dsa_topk_select(logits, k, idx, tl)
+    ts = []
+    for _ in range(30):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        native.dsa_topk_select(logits, k, idx, tl)
+        b.record(st)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    med = statistics.median(ts)
+    nbytes = s_q * n * 2 + s_q * k * 4 + s_q * 4
+    return {"us_per_call_median": med * 1e3, "alg_bytes": nbytes, "alg_gbs": nbytes / (med * 1e-3) / 1e9,
+            "frac_of_hbm_peak": nbytes / (med * 1e-3) / 1e9 / peak_gbs}
+
+
 def cpu_oracle_rate(w, max_seconds: float = 20.0, min_tokens: int = 32):
     """Oracle tokens/s on a bounded prefix of the workload's tokens."""
     import oracle
@@ -360,6 +388,9 @@ def run_native(args):
             if name != args.workload:
                 del ic, oc
                 torch.cuda.empty_cache()
+
+    if not args.skip_sweep and world == 1:
+        per_config["topk_1024x8192_k512"] = time_topk(1024, 8192, 512, flush, peak)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:

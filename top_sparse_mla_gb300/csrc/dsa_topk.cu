@@ -4,15 +4,17 @@
 // it is selected, ties at it go to the lowest-numbered columns, and the selected columns
 // are listed in ascending order).
 //
-// One CTA per row.  The row's bf16 logits become 16-bit keys in shared memory whose
-// unsigned order is the value order: every NaN maps to the largest key (torch.topk
-// ranks NaN above +inf), and -0 maps to +0's key (equal values, equal keys).  Two 8-bit
-// radix-select passes find the k-th largest key T and the number of keys above it.  The
-// row is then cut into 32 contiguous segments, one per warp.  Each warp counts its keys
-// above T and equal to T (ballots, no block barrier).  One prefix over the warps gives
-// each warp the number of columns selected before its segment: those above T, plus the
-// equal ones up to `need`.  Each warp then writes its selected columns in order, so the
-// output is ascending and the first `need` columns equal to T are the lowest-numbered.
+// One CTA of 512 threads per row.  The row's bf16 logits become 16-bit keys in shared
+// memory whose unsigned order is the value order: every NaN maps to the largest key
+// (torch.topk ranks NaN above +inf), and -0 maps to +0's key (equal values, equal keys).
+// Two 8-bit radix-select passes find the k-th largest key T and the number of keys
+// above it: a shared histogram (the first pass while the keys are written), then one
+// warp's suffix scan over the 256 digits.  The
+// row is then read as chunks of eight columns, one chunk per thread and round; a
+// block-wide prefix of the chunks' counts above T and equal to T gives each chunk the
+// number of columns selected before it: those above T, plus the equal ones up to
+// `need`.  Each thread then writes its chunk's selected columns in order, so the output
+// is ascending and the first `need` columns equal to T are the lowest-numbered.
 
 #include <cuda_runtime.h>
 #include <mutex>
@@ -22,7 +24,7 @@
 
 namespace dsa_topk {
 
-constexpr int THREADS = 1024;
+constexpr int THREADS = 512;
 constexpr int WARPS = THREADS / 32;
 
 __device__ __forceinline__ uint32_t order_key(uint32_t b) {
@@ -31,17 +33,50 @@ __device__ __forceinline__ uint32_t order_key(uint32_t b) {
   return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-__global__ void __launch_bounds__(THREADS, 1) topk_kernel(const uint16_t* __restrict__ logits, long long ld,
-                                                          const int32_t* __restrict__ lengths, int n, int k,
-                                                          int32_t* __restrict__ indices,
-                                                          int32_t* __restrict__ topk_length) {
-  extern __shared__ uint16_t s_key[];   // [n]
+// One warp: the digit b with above(b) < kk <= above(b) + hist[b], above(b) being the
+// count of larger digits (1 <= kk <= the histogram's total).  Lane l holds digits
+// 8l .. 8l + 7; a suffix sum over the lanes finds the one lane where the count crosses
+// kk, and that lane scans its eight digits.
+__device__ __forceinline__ void find_digit(const int* hist, int kk, int lane, int* out) {
+  int h[8], tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = hist[8 * lane + i];
+    tot += h[i];
+  }
+  int suf = tot;   // count of digits >= 8 lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  int above = suf - tot;
+  if (above < kk && kk <= suf) {
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+      if (above + h[i] >= kk) {
+        out[0] = 8 * lane + i;
+        out[1] = above;
+        break;
+      }
+      above += h[i];
+    }
+  }
+}
+
+// Two 16-bit keys of one 32-bit word.
+__device__ __forceinline__ uint32_t key_lo(uint32_t w2) { return w2 & 0xFFFFu; }
+__device__ __forceinline__ uint32_t key_hi(uint32_t w2) { return w2 >> 16; }
+
+__global__ void __launch_bounds__(THREADS, 4) topk_kernel(const uint16_t* __restrict__ logits, long long ld,
+                                                       const int32_t* __restrict__ lengths, int n, int k,
+                                                       int32_t* __restrict__ indices,
+                                                       int32_t* __restrict__ topk_length) {
+  extern __shared__ __align__(16) uint16_t s_key[];   // [n rounded up to 8]
   __shared__ int s_hist[256];
-  __shared__ int s_gt[WARPS], s_eq[WARPS];
+  __shared__ int s_wsum[WARPS];
   __shared__ int s_sel[2];
-  static_assert(WARPS == 32, "one warp count per lane");
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const unsigned lt = (1u << lane) - 1u;
   const long long t = blockIdx.x;
   int L = n;
   if (lengths) {
@@ -60,78 +95,112 @@ __global__ void __launch_bounds__(THREADS, 1) topk_kernel(const uint16_t* __rest
     if (tid == 0) topk_length[t] = 0;
     return;
   }
-  const uint16_t* row = logits + t * ld;
-  for (int j = tid; j < L; j += THREADS) s_key[j] = (uint16_t)order_key(row[j]);
-  // pass 1: high byte of the k-th largest key
   for (int i = tid; i < 256; i += THREADS) s_hist[i] = 0;
   __syncthreads();
-  for (int j = tid; j < L; j += THREADS) atomicAdd(&s_hist[s_key[j] >> 8], 1);
-  __syncthreads();
-  if (tid == 0) {
-    int above = 0, b = 255;
-    for (; b > 0; --b) {
-      if (above + s_hist[b] >= k) break;
-      above += s_hist[b];
+  // keys into shared memory, with the histogram of their high bytes (pass 1)
+  const uint16_t* row = logits + t * ld;
+  int j_vec = 0;
+  if (((uintptr_t)row & 15) == 0) {
+    // eight logits per 16-byte load, eight keys per 16-byte store
+    j_vec = L & ~7;
+    for (int j8 = tid; j8 < (L >> 3); j8 += THREADS) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + j8);
+      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t a = order_key(x[e] & 0xFFFFu), b = order_key(x[e] >> 16);
+        o[e] = a | (b << 16);
+        atomicAdd(&s_hist[a >> 8], 1);
+        atomicAdd(&s_hist[b >> 8], 1);
+      }
+      reinterpret_cast<uint4*>(s_key)[j8] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    s_sel[0] = b;
-    s_sel[1] = above;
   }
+  for (int j = j_vec + tid; j < L; j += THREADS) {
+    const uint32_t a = order_key(__ldg(row + j));
+    s_key[j] = (uint16_t)a;
+    atomicAdd(&s_hist[a >> 8], 1);
+  }
+  __syncthreads();
+  if (w == 0) find_digit(s_hist, k, lane, s_sel);
   __syncthreads();
   const int hi = s_sel[0];
   const int above_hi = s_sel[1];
   __syncthreads();
-  // pass 2: low byte, among the keys with that high byte
+  // pass 2: low byte, among the keys with that high byte (eight keys per 16-byte read)
   for (int i = tid; i < 256; i += THREADS) s_hist[i] = 0;
   __syncthreads();
-  for (int j = tid; j < L; j += THREADS) {
-    const int key = s_key[j];
-    if ((key >> 8) == hi) atomicAdd(&s_hist[key & 255], 1);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int above = above_hi, b = 255;
-    for (; b > 0; --b) {
-      if (above + s_hist[b] >= k) break;
-      above += s_hist[b];
+  const int L8 = (L + 7) >> 3;
+  for (int ci = tid; ci < L8; ci += THREADS) {
+    const uint4 kv = reinterpret_cast<const uint4*>(s_key)[ci];
+    const uint32_t x[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t key = (e & 1) ? key_hi(x[e >> 1]) : key_lo(x[e >> 1]);
+      if (8 * ci + e < L && (int)(key >> 8) == hi) atomicAdd(&s_hist[key & 255], 1);
     }
-    s_sel[0] = b;
-    s_sel[1] = above;
   }
   __syncthreads();
-  const int T = (hi << 8) | s_sel[0];
-  const int need = k - s_sel[1];   // columns equal to T to take, lowest first
-  // segment of warp w: columns [c_begin, c_end), a multiple of 32 long
-  const int seg = ((L + THREADS - 1) / THREADS) * 32;
-  const int c_begin = w * seg;
-  const int c_end = min(c_begin + seg, L);
-  int gt = 0, eq = 0;
-  for (int c = c_begin; c < c_end; c += 32) {
-    const int j = c + lane;
-    const int key = j < c_end ? (int)s_key[j] : -1;
-    gt += __popc(__ballot_sync(0xFFFFFFFFu, key > T));
-    eq += __popc(__ballot_sync(0xFFFFFFFFu, key == T));
-  }
-  if (lane == 0) {
-    s_gt[w] = gt;
-    s_eq[w] = eq;
-  }
+  if (w == 0) find_digit(s_hist, k - above_hi, lane, s_sel);
   __syncthreads();
-  // columns before this segment: above T, and equal to T
-  const int gt_before = __reduce_add_sync(0xFFFFFFFFu, lane < w ? s_gt[lane] : 0);
-  const int eq_before = __reduce_add_sync(0xFFFFFFFFu, lane < w ? s_eq[lane] : 0);
-  int eq_run = eq_before;
-  int sel_run = gt_before + min(eq_before, need);
-  for (int c = c_begin; c < c_end; c += 32) {
-    const int j = c + lane;
-    const int key = j < c_end ? (int)s_key[j] : -1;
-    const bool e = key == T;
-    const unsigned be = __ballot_sync(0xFFFFFFFFu, e);
-    const bool sel = key > T || (e && eq_run + __popc(be & lt) < need);
-    const unsigned bs = __ballot_sync(0xFFFFFFFFu, sel);
-    const int pos = sel_run + __popc(bs & lt);
-    if (sel && pos < k) out[pos] = j;
-    eq_run += __popc(be);
-    sel_run += __popc(bs);
+  const uint32_t T = (uint32_t)((hi << 8) | s_sel[0]);
+  const int need = k - above_hi - s_sel[1];   // columns equal to T to take, lowest first
+  // Output in column order.  Chunk ci (eight columns) belongs to thread ci % THREADS in
+  // round ci / THREADS; per round a block-wide exclusive prefix of the chunks' counts
+  // above T and equal to T (packed in one int: at most 8 x THREADS each) places them.
+  int gt_base = 0, eq_base = 0;   // counts of earlier rounds
+  for (int c0 = 0; c0 < L8; c0 += THREADS) {
+    const int ci = c0 + tid;
+    uint32_t x[4] = {0u, 0u, 0u, 0u};
+    if (ci < L8) {
+      const uint4 kv = reinterpret_cast<const uint4*>(s_key)[ci];
+      x[0] = kv.x; x[1] = kv.y; x[2] = kv.z; x[3] = kv.w;
+    }
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t key = (e & 1) ? key_hi(x[e >> 1]) : key_lo(x[e >> 1]);
+      const bool in = ci < L8 && 8 * ci + e < L;
+      gt += (in && key > T) ? 1 : 0;
+      eq += (in && key == T) ? 1 : 0;
+    }
+    const int packed = (gt << 16) | eq;
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[w] = incl;
+    __syncthreads();
+    int wbefore = 0, total = 0;
+#pragma unroll
+    for (int u = 0; u < WARPS; ++u) {
+      const int sv = s_wsum[u];
+      wbefore += u < w ? sv : 0;
+      total += sv;
+    }
+    __syncthreads();   // s_wsum is rewritten by the next round
+    const int excl = wbefore + incl - packed;
+    int gtb = gt_base + (excl >> 16), eqb = eq_base + (excl & 0xFFFF);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t key = (e & 1) ? key_hi(x[e >> 1]) : key_lo(x[e >> 1]);
+      const int col = 8 * ci + e;
+      if (ci < L8 && col < L) {
+        if (key > T) {
+          const int pos = gtb + min(eqb, need);
+          if (pos < k) out[pos] = col;
+          ++gtb;
+        } else if (key == T) {
+          if (eqb < need && gtb + eqb < k) out[gtb + eqb] = col;
+          ++eqb;
+        }
+      }
+    }
+    gt_base += total >> 16;
+    eq_base += total & 0xFFFF;
   }
   if (tid == 0) topk_length[t] = k;
 }
@@ -169,7 +238,7 @@ extern "C" int dsa_topk_select(const void* logits, int64_t ld, const int32_t* le
       attr_done[dev] = true;
     }
   }
-  const size_t smem = (size_t)n * sizeof(uint16_t);
+  const size_t smem = (size_t)((n + 7) & ~7) * sizeof(uint16_t);
   topk_kernel<<<(unsigned)s_q, THREADS, smem, (cudaStream_t)stream>>>(
       (const uint16_t*)logits, (long long)ld, lengths, n, k, indices, topk_length);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
