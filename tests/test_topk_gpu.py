@@ -40,7 +40,8 @@ def _tied(rng, s_q, n, step=0.125):
     return torch.tensor(np.round(rng.normal(size=(s_q, n)) / step) * step, dtype=torch.bfloat16)
 
 
-@pytest.mark.parametrize("n,k", [(1, 1), (7, 3), (100, 64), (1000, 640), (4097, 2048), (20000, 512), (65536, 2048)])
+@pytest.mark.parametrize("n,k", [(1, 1), (7, 3), (100, 64), (1000, 640), (4097, 2048), (8192, 512), (8193, 512),
+                                 (20000, 512), (65536, 2048)])
 def test_random_rows_with_ties(n, k):
     rng = np.random.default_rng(n + k)
     _check(_tied(rng, 5, n), k)
@@ -51,6 +52,12 @@ def test_ragged_lengths_and_padded_rows():
     n = 3000
     x = _tied(rng, 8, n, step=0.5)
     _check(x, 700, lengths=[3000, 700, 699, 0, -3, 5000, 1, 1500], pad=40)
+    # an odd row pitch: rows start off the 16-byte grid (element loads instead of vectors)
+    _check(x, 700, lengths=[3000, 701, 2999, 33, 64, 5000, 31, 1500], pad=3)
+    # rows of the register path's boundary length, and one past it (the shared-memory path)
+    for n2 in (8192, 8193):
+        y = _tied(rng, 4, n2, step=0.25)
+        _check(y, 512, lengths=[n2, 4000, 513, n2 - 1], pad=5)
 
 
 def test_special_values():

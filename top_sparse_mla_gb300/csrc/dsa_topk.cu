@@ -4,17 +4,23 @@
 // it is selected, ties at it go to the lowest-numbered columns, and the selected columns
 // are listed in ascending order).
 //
-// One CTA of 512 threads per row.  The row's bf16 logits become 16-bit keys in shared
-// memory whose unsigned order is the value order: every NaN maps to the largest key
-// (torch.topk ranks NaN above +inf), and -0 maps to +0's key (equal values, equal keys).
-// Two 8-bit radix-select passes find the k-th largest key T and the number of keys
-// above it: a shared histogram (the first pass while the keys are written), then one
-// warp's suffix scan over the 256 digits.  The
-// row is then read as chunks of eight columns, one chunk per thread and round; a
-// block-wide prefix of the chunks' counts above T and equal to T gives each chunk the
-// number of columns selected before it: those above T, plus the equal ones up to
-// `need`.  Each thread then writes its chunk's selected columns in order, so the output
-// is ascending and the first `need` columns equal to T are the lowest-numbered.
+// One CTA per row.  The row's bf16 logits become 16-bit keys whose unsigned order is the
+// value order: every NaN maps to the largest key (torch.topk ranks NaN above +inf), and
+// -0 maps to +0's key (equal values, equal keys).  Two 8-bit radix-select passes find the
+// k-th largest key T and the number of keys above it: a shared histogram of the high
+// bytes, one warp's suffix scan over the 256 digits, then the same over the low bytes of
+// the keys in the chosen high-byte bin.
+//
+// Rows of up to 8192 columns (the register path): 256 threads, each holding the keys of
+// 32 consecutive columns in registers.  After the passes each thread has one bit mask of
+// its columns above T and one of those equal to T; a block-wide exclusive prefix of the
+// packed counts gives each thread the number of columns selected before its own (those
+// above T, plus the equal ones up to `need`), and it writes its selected columns in
+// order, so the output is ascending and the first `need` columns equal to T are the
+// lowest-numbered.
+//
+// Longer rows (up to 65536 columns): 512 threads, the keys in shared memory, the same two
+// passes, and the placement taken in rounds of 512 chunks of eight columns.
 
 #include <cuda_runtime.h>
 #include <mutex>
@@ -26,6 +32,8 @@ namespace dsa_topk {
 
 constexpr int THREADS = 512;
 constexpr int WARPS = THREADS / 32;
+// the register path: RT threads of RK columns each, RB CTAs per SM
+constexpr int RT = 256, RK = 32, RB = 4;
 
 __device__ __forceinline__ uint32_t order_key(uint32_t b) {
   if ((b & 0x7F80u) == 0x7F80u && (b & 0x007Fu) != 0u) return 0xFFFFu;   // NaN, any sign or payload
@@ -205,6 +213,153 @@ __global__ void __launch_bounds__(THREADS, 4) topk_kernel(const uint16_t* __rest
   if (tid == 0) topk_length[t] = k;
 }
 
+// Keys of the two bf16 values of one 32-bit word at once (the same map as order_key):
+// the sign selects XOR 0xFFFF or 0x8000 per half; -0 then reads 0x7FFF and is moved to
+// +0's 0x8000; a NaN half (magnitude bits above 0x7F80) becomes 0xFFFF.
+__device__ __forceinline__ uint32_t order_key2(uint32_t x) {
+  const uint32_t s = (x >> 15) & 0x00010001u;
+  uint32_t kk = x ^ (s * 0x7FFFu | 0x80008000u);
+  // -0 came out as 0x7FFF (no other value does): +0's key
+  if ((kk & 0xFFFFu) == 0x7FFFu) kk += 1u;
+  if ((kk >> 16) == 0x7FFFu) kk += 0x10000u;
+  // NaN (|bits| above 0x7F80) -> 0xFFFF
+  const uint32_t nan = ((x & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u;
+  return kk | ((nan >> 15) * 0xFFFFu);
+}
+
+// Register path (n <= NT * KPT): thread i owns columns KPT i .. KPT i + KPT - 1 and keeps
+// their keys in registers, one per register.
+template <int NT, int KPT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) topk_reg_kernel(const uint16_t* __restrict__ logits, long long ld,
+                                                          const int32_t* __restrict__ lengths, int n, int k,
+                                                          int32_t* __restrict__ indices,
+                                                          int32_t* __restrict__ topk_length) {
+  static_assert(KPT <= 32 && KPT % 8 == 0, "one 32-bit mask per thread; whole 16-byte loads");
+  static_assert(NT >= 256 && NT <= 1024 && NT % 32 == 0, "one thread per histogram bin when clearing");
+  constexpr int NWARP = NT / 32;
+  __shared__ int s_hist[2][256];
+  __shared__ int s_wsum[NWARP];
+  __shared__ int s_sel[4];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const long long t = blockIdx.x;
+  int L = n;
+  if (lengths) {
+    const int l = lengths[t];
+    L = l < 0 ? 0 : (l > n ? n : l);
+  }
+  int32_t* out = indices + t * (long long)k;
+  if (L <= k) {
+    for (int j = tid; j < k; j += NT) out[j] = j < L ? j : -1;
+    if (tid == 0) topk_length[t] = L;
+    return;
+  }
+  if (k == 0) {
+    if (tid == 0) topk_length[t] = 0;
+    return;
+  }
+  for (int i = tid; i < 512; i += NT) (&s_hist[0][0])[i] = 0;
+  const int c0 = KPT * tid;
+  const int nv = L - c0 < 0 ? 0 : (L - c0 > KPT ? KPT : L - c0);   // valid columns of this thread
+  const bool full = nv == KPT;
+  const uint16_t* row = logits + t * ld;
+  uint32_t key[KPT];   // one key per register; invalid slots hold 0, below every valid key
+  if (full && ((uintptr_t)(row + c0) & 15) == 0) {
+#pragma unroll
+    for (int v = 0; v < KPT / 8; ++v) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + c0) + v);
+      const uint32_t x[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t kk = order_key2(x[e]);
+        key[8 * v + 2 * e] = kk & 0xFFFFu;
+        key[8 * v + 2 * e + 1] = kk >> 16;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT / 2; ++i) {
+      const uint32_t a = 2 * i < nv ? (uint32_t)__ldg(row + c0 + 2 * i) : 0u;
+      const uint32_t b = 2 * i + 1 < nv ? (uint32_t)__ldg(row + c0 + 2 * i + 1) : 0u;
+      const uint32_t kk = order_key2(a | (b << 16));
+      key[2 * i] = 2 * i < nv ? (kk & 0xFFFFu) : 0u;
+      key[2 * i + 1] = 2 * i + 1 < nv ? (kk >> 16) : 0u;
+    }
+  }
+  __syncthreads();
+  // pass 1: high bytes of the valid keys
+  if (full) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) atomicAdd(&s_hist[0][key[e] >> 8], 1);
+  } else {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if (e < nv) atomicAdd(&s_hist[0][key[e] >> 8], 1);
+  }
+  __syncthreads();
+  if (w == 0) find_digit(s_hist[0], k, lane, s_sel);
+  __syncthreads();
+  const uint32_t hi = (uint32_t)s_sel[0];
+  const int above_hi = s_sel[1];
+  // pass 2: low bytes of the keys with that high byte (an invalid slot's key 0 can
+  // match only if hi is 0; then it is skipped by its column)
+  if (full || hi != 0u) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if ((key[e] >> 8) == hi) atomicAdd(&s_hist[1][key[e] & 255u], 1);
+  } else {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if (e < nv && (key[e] >> 8) == hi) atomicAdd(&s_hist[1][key[e] & 255u], 1);
+  }
+  __syncthreads();
+  if (w == 0) find_digit(s_hist[1], k - above_hi, lane, s_sel + 2);
+  __syncthreads();
+  const uint32_t T = (hi << 8) | (uint32_t)s_sel[2];
+  const int need = k - above_hi - s_sel[3];
+  // T >= 1 (the k-th largest valid key is a valid key), so an invalid slot's 0 is in
+  // neither mask
+  uint32_t gtm = 0u, eqm = 0u;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    gtm |= (key[e] > T) ? (1u << e) : 0u;
+    eqm |= (key[e] == T) ? (1u << e) : 0u;
+  }
+  // block-wide exclusive prefix of (above T) << 16 | (equal to T), in column order
+  const int packed = (__popc(gtm) << 16) | __popc(eqm);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[w] = incl;
+  __syncthreads();
+  int ws = lane < NWARP ? s_wsum[lane] : 0;
+#pragma unroll
+  for (int o = 1; o < NWARP; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, ws, o);
+    if (lane >= o) ws += v;
+  }
+  const int wbefore = __shfl_sync(0xFFFFFFFFu, ws, (w + 31) & 31);
+  const int excl = (w > 0 ? wbefore : 0) + incl - packed;
+  int gtb = excl >> 16, eqb = excl & 0xFFFF;
+  uint32_t m = gtm | eqm;
+  while (m) {
+    const int e = __ffs(m) - 1;
+    m &= m - 1u;
+    const int col = c0 + e;
+    if ((gtm >> e) & 1u) {
+      const int pos = gtb + min(eqb, need);
+      if (pos < k) out[pos] = col;
+      ++gtb;
+    } else {
+      if (eqb < need && gtb + eqb < k) out[gtb + eqb] = col;
+      ++eqb;
+    }
+  }
+  if (tid == 0) topk_length[t] = k;
+}
+
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 }  // namespace dsa_topk
@@ -237,6 +392,11 @@ extern "C" int dsa_topk_select(const void* logits, int64_t ld, const int32_t* le
         return DSA_ERR_CUDA;
       attr_done[dev] = true;
     }
+  }
+  if (n <= RT * RK) {
+    topk_reg_kernel<RT, RK, RB><<<(unsigned)s_q, RT, 0, (cudaStream_t)stream>>>(
+        (const uint16_t*)logits, (long long)ld, lengths, n, k, indices, topk_length);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   const size_t smem = (size_t)((n + 7) & ~7) * sizeof(uint16_t);
   topk_kernel<<<(unsigned)s_q, THREADS, smem, (cudaStream_t)stream>>>(
