@@ -19,9 +19,11 @@ Modules:
   brute       -- a scalar pure-Python restatement for tiny inputs (cross-check)
   topk        -- the index producer's top-k column selection (vLLM PR #64364, Claims
                  and Validation)
+  kv_insert   -- the KV-cache insert: norm, RoPE and fp8_ds_mla quantisation of new rows
+                 (vLLM PR #64364, "The changes and what each bought", Attention)
 """
 
-from . import codecs, sparse_mla, brute, topk  # noqa: F401
+from . import codecs, sparse_mla, brute, topk, kv_insert  # noqa: F401
 from .sparse_mla import (  # noqa: F401
     OracleParams,
     decode_kv_rows,

@@ -109,6 +109,22 @@ def bf16_decode(bits) -> np.ndarray:
         return b.view(np.float32).astype(np.float64)
 
 
+def bf16_encode(x) -> np.ndarray:
+    """Round float64 values to bfloat16 bit patterns (uint16): round-to-nearest-even on
+    the binary32 value's upper half.  x is first rounded to binary32 (the values this
+    oracle rounds are binary32 or exact in it); NaN gives the quiet NaN 0x7FC0, +-inf stay
+    infinite.
+
+    Format: bfloat16, the rope part of a cache row written by the KV insert.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint32)
+    r = np.where(np.isnan(f), 0x7FC0, r)
+    return r.astype(np.uint16)
+
+
 def fp32_decode_le(raw) -> np.ndarray:
     """Little-endian IEEE binary32 from a uint8 array whose last axis is a multiple of 4.
 

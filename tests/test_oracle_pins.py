@@ -316,3 +316,18 @@ def test_index_out_of_range_is_an_error():
     w.indices[0, 5] = 16
     with pytest.raises(IndexError):
         _run(w)
+
+
+def test_bf16_encode_matches_torch_rounding():
+    # round to nearest even on the binary32 value, as torch's float32 -> bfloat16 cast
+    import torch
+    from oracle import codecs as C
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(50000) * np.exp2(rng.integers(-60, 60, 50000))).astype(np.float32).astype(np.float64)
+    x = np.concatenate([x, [0.0, -0.0, np.inf, -np.inf, 3.3895313892515355e38, 3.4e38, 1e-40, -1e-45, 1.00390625,
+                            1.01171875, -1.00390625]])
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    assert np.array_equal(C.bf16_encode(x), ref)
+    assert C.bf16_encode(np.array([np.nan]))[0] == 0x7FC0
+    # ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 and goes to the even 1
+    assert C.bf16_encode(np.array([1.00390625]))[0] == 0x3F80
