@@ -275,6 +275,37 @@ def time_topk(s_q: int, n: int, k: int, flush, peak_gbs: float):
             "frac_of_hbm_peak": nbytes / (med * 1e-3) / 1e9 / peak_gbs}
 
 
+def time_kv_insert(n: int, n_rows: int, flush, peak_gbs: float):
+    """The KV-cache insert (include/dsa_kv_insert.h): n seeded N(0,1) bf16 KV rows
+    normalised, roped and quantised into random distinct rows of an n_rows-row pool;
+    median CUDA-event time of 30 calls, L2 flushed before each.  Bytes: the KV rows, the
+    positions and slots read, the 656-byte rows written."""
+    import torch
+    from top_sparse_mla_gb300 import native
+    g = torch.Generator(device="cuda").manual_seed(9)
+    kv = torch.randn((n, 576), generator=g, device="cuda").to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn((512,), generator=g, device="cuda")).to(torch.bfloat16)
+    pos = torch.randint(0, 32768, (n,), generator=g, device="cuda", dtype=torch.int32)
+    slots = torch.randperm(n_rows, generator=g, device="cuda")[:n].to(torch.int64)
+    pool = torch.zeros((n_rows, 656), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        native.dsa_kv_insert(kv, pos, slots, w, pool)
+    ts = []
+    for _ in range(30):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        native.dsa_kv_insert(kv, pos, slots, w, pool)
+        b.record(st)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    med = statistics.median(ts)
+    nbytes = n * (576 * 2 + 4 + 8 + 656) + 512 * 2
+    return {"us_per_call_median": med * 1e3, "alg_bytes": nbytes, "alg_gbs": nbytes / (med * 1e-3) / 1e9,
+            "frac_of_hbm_peak": nbytes / (med * 1e-3) / 1e9 / peak_gbs, "tokens": n, "pool_rows": n_rows}
+
+
 def cpu_oracle_rate(w, max_seconds: float = 20.0, min_tokens: int = 32):
     """Oracle tokens/s on a bounded prefix of the workload's tokens."""
     import oracle
@@ -391,6 +422,8 @@ def run_native(args):
 
     if not args.skip_sweep and world == 1:
         per_config["topk_1024x8192_k512"] = time_topk(1024, 8192, 512, flush, peak)
+        per_config["kv_insert_4096_into_1M_rows"] = time_kv_insert(4096, 1 << 20, flush, peak)
+        per_config["kv_insert_65536_into_1M_rows"] = time_kv_insert(65536, 1 << 20, flush, peak)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:

@@ -83,6 +83,35 @@ def test_topk_select_checks_arguments_before_the_device(lib):
     assert f(fake, 100, None, 4, 100, 8, fake, fake, None) in (native.DSA_ERR_CUDA, native.DSA_ERR_UNSUPPORTED_DEVICE)
 
 
+def test_kv_insert_checks_arguments_before_the_device(lib):
+    ok, bad = native.DSA_OK, native.DSA_ERR_INVALID_ARG
+    fake = 1 << 20   # a 16-byte aligned address that is never dereferenced on the host
+    f = lib.dsa_kv_insert
+    args = dict(kv=fake, ld=576, pos=fake, slots=fake, n=4, w=fake, eps=1e-6, base=10000.0, pool=fake, rows=100,
+                flags=0, status=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["kv"], a["ld"], a["pos"], a["slots"], a["n"], a["w"], a["eps"], a["base"], a["pool"], a["rows"],
+                 a["flags"], a["status"], None)
+
+    assert call(n=-1) == bad
+    assert call(ld=575) == bad and call(ld=580) == bad          # ld >= 576 and a multiple of 8
+    assert call(eps=-1.0) == bad and call(eps=float("nan")) == bad
+    assert call(base=0.0) == bad and call(base=float("inf")) == bad
+    assert call(flags=2) == bad                                 # only DSA_KV_FLAG_CHECK_SLOTS is defined
+    assert call(rows=-1) == bad
+    assert call(kv=None) == bad and call(slots=None) == bad and call(w=None) == bad and call(pos=None) == bad
+    assert call(pool=None) == bad                              # rows > 0 needs a pool
+    assert call(kv=fake + 8) == bad and call(w=fake + 2) == bad and call(pool=fake + 4) == bad
+    assert call(slots=fake + 4) == bad and call(status=fake + 2) == bad
+    assert call(n=0, kv=None) == ok                             # an empty batch is a no-op
+    # valid arguments reach the device check, which fails without a GPU
+    assert call() in (native.DSA_ERR_CUDA, native.DSA_ERR_UNSUPPORTED_DEVICE)
+    assert call(flags=native.DSA_KV_FLAG_CHECK_SLOTS, status=fake) in (native.DSA_ERR_CUDA,
+                                                                         native.DSA_ERR_UNSUPPORTED_DEVICE)
+
+
 def test_params_init_defaults(lib):
     p = native.dsa_params_init(4, 64, 640, 128, 1000, 2000)
     assert (p.s_q, p.h_q, p.topk, p.n_swa_cols, p.n_swa_rows, p.n_cmp_rows) == (4, 64, 640, 128, 1000, 2000)

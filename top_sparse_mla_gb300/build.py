@@ -9,7 +9,7 @@ import sys
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
-SOURCES = [os.path.join(PKG_DIR, "csrc", "dsa_sparse_attn.cu"), os.path.join(PKG_DIR, "csrc", "dsa_topk.cu")]
+SOURCES = [os.path.join(PKG_DIR, "csrc", f) for f in ("dsa_sparse_attn.cu", "dsa_topk.cu", "dsa_kv_insert.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libdsa_sparse_attn.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
@@ -26,7 +26,8 @@ def nvcc_path() -> str:
 def build(verbose: bool = False, extra_flags=None) -> str:
     """Build the shared library if any source is newer than it; return its path."""
     deps = SOURCES + [os.path.join(PKG_DIR, "csrc", "ptx_sm103.cuh"), os.path.join(INCLUDE, "dsa_sparse_attn.h"),
-                      os.path.join(INCLUDE, "dsa_topk.h"), os.path.abspath(__file__)]
+                      os.path.join(INCLUDE, "dsa_topk.h"), os.path.join(INCLUDE, "dsa_kv_insert.h"),
+            os.path.abspath(__file__)]
     if os.path.exists(LIB_PATH) and all(os.path.getmtime(LIB_PATH) >= os.path.getmtime(d) for d in deps):
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"

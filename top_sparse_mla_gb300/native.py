@@ -32,6 +32,8 @@ DSA_TOPK_MAX_COLS = 65536
 DSA_TOPK_MAX_K = 2048
 DSA_ROW_BYTES = 656
 DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
+DSA_KV_FLAG_CHECK_SLOTS = 1
+DSA_STATUS_SLOT_OUT_OF_RANGE = 4
 
 EXPORTED = (
     "dsa_params_init",
@@ -43,6 +45,7 @@ EXPORTED = (
     "dsa_sparse_attn_num_splits",
     "dsa_error_string",
     "dsa_topk_select",
+    "dsa_kv_insert",
 )
 
 
@@ -99,6 +102,9 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_error_string.restype = ctypes.c_char_p
     lib.dsa_topk_select.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp]
     lib.dsa_topk_select.restype = ctypes.c_int
+    lib.dsa_kv_insert.argtypes = [vp, ctypes.c_int64, vp, vp, ctypes.c_int32, vp, ctypes.c_float, ctypes.c_float, vp,
+                                  ctypes.c_int64, ctypes.c_uint32, vp, vp]
+    lib.dsa_kv_insert.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -184,6 +190,23 @@ def dsa_topk_select(logits, k: int, indices, topk_length, lengths=None, stream=N
                                    _ptr(topk_length), _stream(stream))
     if rc != DSA_OK:
         raise DsaError(rc, "dsa_topk_select")
+
+
+def dsa_kv_insert(kv, positions, slots, kv_norm_w, pool, rms_eps: float = 1e-6, rope_base: float = 10000.0,
+                  check_slots: bool = False, status=None, stream=None) -> None:
+    """KV-cache insert (include/dsa_kv_insert.h). kv: bf16 [s_new, ld >= 576] device tensor
+    (512 latent then 64 rotary values per row); positions: int32 [s_new]; slots: int64
+    [s_new] (< 0 = skip); kv_norm_w: bf16 [512]; pool: uint8 [n_rows, 656]; status: uint32
+    [1] device tensor or None."""
+    s_new = int(kv.shape[0])
+    if s_new > 0 and int(kv.stride(1)) != 1:
+        raise DsaError(DSA_ERR_INVALID_ARG, "dsa_kv_insert: kv rows must be contiguous")
+    ld = int(kv.stride(0)) if s_new > 0 else 576
+    rc = library().dsa_kv_insert(_ptr(kv), ld, _ptr(positions), _ptr(slots), s_new, _ptr(kv_norm_w),
+                                 float(rms_eps), float(rope_base), _ptr(pool), int(pool.shape[0]),
+                                 DSA_KV_FLAG_CHECK_SLOTS if check_slots else 0, _ptr(status), _stream(stream))
+    if rc != DSA_OK:
+        raise DsaError(rc, "dsa_kv_insert")
 
 
 def dsa_sparse_attn_read_status(workspace, stream=None) -> int:
