@@ -12,9 +12,10 @@
  *   - y = x / sqrt(mean(x^2) + rms_eps) * kv_norm_w, over the 512 latent dims, with
  *     fp32 statistics (the rotary dims are not normalised);
  *   - per 128-dim block b: s_b = max|y_b| / 448 in fp32 (1 for an all-zero block), and
- *     the E4M3 code of each value is round-to-nearest-even of 448 * (x*w) / max_b|x*w|,
- *     taken as one binary32 division (x*w is exact in binary32; this equals y / s_b
- *     without the rounding of the RMS factor);
+ *     the E4M3 code of each value is round-to-nearest-even of (x*w) * (448 / m_b),
+ *     m_b = max_b|x*w|, in binary32: one rounded quotient per block and one rounded
+ *     product per value (x*w and m_b are exact in binary32; in exact arithmetic this is
+ *     y / s_b, here without the rounding of the RMS factor);
  *   - r rotated by positions[i] * rope_base^(-2j/64) on the interleaved pairs
  *     (2j, 2j + 1), as the attention rotates q, then rounded to bf16 (nearest even);
  *   - row slots[i] of `pool` := the 512 codes, the 4 scales s_b (fp32, little-endian),

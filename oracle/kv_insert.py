@@ -16,9 +16,10 @@ one an MLA KV projection fixes, written out here):
 4. The latent part is quantised per 128-dim block as the cache format stores it: fp32
    scale = max|y| / 448 (1 for an all-zero block), E4M3 codes of y / scale (round to
    nearest even).  The code is an integer decided by floating point, so it is decided in
-   the precision the kernel uses: y / scale equals 448 * (x*w) / max|x*w| exactly (the
-   RMS factor cancels), and that ratio is taken as one binary32 division of exact
-   binary32 operands (x*w is exact: two 8-bit significands), then rounded to E4M3.
+   the precision the kernel uses: y / scale equals (x*w) * (448 / max|x*w|) exactly (the
+   RMS factor cancels), taken in binary32 as one rounded quotient 448 / max|x*w| per block
+   and one rounded product per value (x*w is exact: two 8-bit significands), then rounded
+   to E4M3.
 5. The rotary part is stored as bf16 (round to nearest even); the row is 512 codes, 4
    little-endian fp32 scales and 64 bf16 values (656 bytes).
 6. slots[i] < 0 skips token i (a padding token); every other row of the pool is left as
@@ -46,7 +47,8 @@ def quantise_latent(x_bits: np.ndarray, w_bits: np.ndarray, eps: float):
     """Step 4: (codes uint8 [n, 512], scales float64 [n, 4]) of the normalised latent.
 
     The scales are float64 values of max|y| / 448; the codes follow point 4 of the module
-    docstring (the ratio 448 * (x*w) / max|x*w| as one binary32 division).
+    docstring ((x*w) * (448 / max|x*w|), one binary32 quotient per block, one binary32
+    product per value).
     """
     y = normalised_latent(x_bits, w_bits, eps)
     n = y.shape[0]
@@ -60,7 +62,8 @@ def quantise_latent(x_bits: np.ndarray, w_bits: np.ndarray, eps: float):
         nz = m[:, 0] > 0
         scales[nz, b] = amax_y[nz] / E4M3_MAX
         with np.errstate(invalid="ignore", divide="ignore"):
-            ratio = (np.float32(E4M3_MAX) * xw[:, blk]) / np.where(m > 0, m, np.float32(1))  # binary32 ops
+            r = np.float32(E4M3_MAX) / np.where(m > 0, m, np.float32(1))                      # binary32 quotient
+        ratio = xw[:, blk] * r                                                                # binary32 product
         ratio = np.where(m > 0, ratio, np.float32(0)).astype(np.float64)
         codes[:, blk] = codecs.e4m3_encode(ratio)
     return codes, scales

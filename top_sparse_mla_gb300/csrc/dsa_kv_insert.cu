@@ -79,13 +79,15 @@ __global__ void __launch_bounds__(32 * WARPS) kv_insert_kernel(const __grid_cons
   for (int o = 4; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   const float inv = 1.0f / sqrtf(ss * (1.0f / D_LAT) + P.eps);
 
-  // codes: round-to-nearest-even E4M3 of 448 * (x * w) / m, one binary32 division each
+  // codes: round-to-nearest-even E4M3 of (x * w) * (448 / m): one rounded quotient per
+  // block, one rounded product per value (no contraction into anything else)
+  const float rq = m > 0.f ? __fdiv_rn(448.0f, m) : 0.f;
   uint32_t cw[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     float q[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) q[e] = m > 0.f ? __fdiv_rn(448.0f * xw[4 * k + e], m) : 0.f;
+    for (int e = 0; e < 4; ++e) q[e] = __fmul_rn(xw[4 * k + e], rq);
     cw[k] = dsa::f32x2_to_e4m3x2(q[0], q[1]) | (dsa::f32x2_to_e4m3x2(q[2], q[3]) << 16);
   }
   // the block's scale: max|y| / 448 = m * inv / 448
