@@ -2,8 +2,9 @@
 (oracle/kv_insert.py), on seeded inputs.
 
 What must agree, and why:
-- E4M3 codes bit for bit: both sides take each code as one binary32 division of exact
-  binary32 operands, 448 * (x*w) / max|x*w|, rounded to nearest even;
+- E4M3 codes bit for bit: both sides take each code in binary32 as (x*w) times one
+  rounded quotient 448 / max|x*w| per block (x*w and the max are exact), rounded to
+  nearest even;
 - the fp32 block scales within 2^-20 relative: the kernel's fp32 RMS statistics
   (a sum of 512 squares and a square root) against the oracle's float64;
 - the rotated bf16 rope values within one bf16 step plus 2^-20 of the pair's length (the
