@@ -84,6 +84,17 @@ extern "C" {
  * its other splits give up their bounded wait for it (also DSA_STATUS_WAIT_TIMEOUT),
  * so token 0's output is left unwritten, and the other tokens are complete. */
 #define DSA_FLAG_TEST_WAIT_TIMEOUT 2u
+/* Launch after a producer kernel without a gap: the call's first kernel (the queue
+ * order kernel; the queue path is taken without splits and up to DSA_ORDER_MAX_TOKENS
+ * tokens) is launched as a programmatic dependent of the kernel enqueued just before
+ * it on `stream`, for example dsa_kv_insert or dsa_topk_select, which let their
+ * dependents launch early.  It starts while that kernel is still running and waits for
+ * its completion (griddepcontrol.wait) before it reads anything, so every input the
+ * producer writes (pool rows, indices, lengths) is complete before it is read.  On the
+ * split path, and in dsa_sparse_attn_fwd_noalloc, the workspace is cleared by a memset
+ * first, which orders the call after the producer as usual; the flag then changes
+ * nothing. */
+#define DSA_FLAG_AFTER_PRODUCER 4u
 
 #define DSA_STATUS_INDEX_OUT_OF_RANGE 1u /* an index was >= its pool size (with the flag) */
 #define DSA_STATUS_WAIT_TIMEOUT 2u       /* an on-chip pipeline wait gave up; output invalid */

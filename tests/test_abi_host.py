@@ -56,11 +56,12 @@ def test_order_bound_matches_the_kernel_source():
 
 
 def test_flag_mask(lib):
-    # both defined flags pass the argument check (num_splits returns 0 on a bad argument)
+    # the defined flags pass the argument check (num_splits returns 0 on a bad argument)
     p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096,
-                               flags=native.DSA_FLAG_CHECK_INDICES | native.DSA_FLAG_TEST_WAIT_TIMEOUT)
+                               flags=native.DSA_FLAG_CHECK_INDICES | native.DSA_FLAG_TEST_WAIT_TIMEOUT
+                               | native.DSA_FLAG_AFTER_PRODUCER)
     assert native.dsa_sparse_attn_num_splits(p, 152) == 8
-    for bad in (4, 8, 1 << 31):
+    for bad in (8, 16, 1 << 31):
         p.flags = bad
         assert native.dsa_sparse_attn_num_splits(p, 152) == 0
 

@@ -44,6 +44,9 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 __global__ void __launch_bounds__(32 * WARPS) kv_insert_kernel(const __grid_constant__ Params P) {
+  // a dependent launched with programmatic serialization may start now; it waits for
+  // this kernel's completion before it reads the pool (DSA_FLAG_AFTER_PRODUCER)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long i = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (i >= P.s_new) return;

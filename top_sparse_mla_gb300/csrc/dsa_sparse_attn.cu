@@ -1263,6 +1263,9 @@ __global__ void __launch_bounds__(ORDER_THREADS, 1) dsa_order_kernel(const int32
   __shared__ int s_cnt[NW][NK];   // per warp: tokens of each count in the current chunk
   __shared__ int s_off[NW][NK];   // per warp: where those tokens go
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // launched as a producer's programmatic dependent (DSA_FLAG_AFTER_PRODUCER): nothing is
+  // read before that kernel has completed; a no-op otherwise
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const unsigned lt = (1u << lane) - 1u;
   auto key = [&](int t) {
@@ -1469,7 +1472,8 @@ static int check_params(const dsa_params* p) {
   if (p->topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
   if (!(p->softmax_scale == p->softmax_scale) || !(p->rope_base > 0.f) || !(p->rms_eps >= 0.f))
     return DSA_ERR_INVALID_ARG;
-  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT)) return DSA_ERR_INVALID_ARG;
+  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_AFTER_PRODUCER))
+    return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
 
@@ -1538,8 +1542,18 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   const bool ordered = ns == 1 && p->s_q <= ORDER_MAX_TOKENS;
   if (ordered) {
     // header and the queue's order (in the counters' region, which the queue path does not use)
-    dsa_order_kernel<<<1, ORDER_THREADS, 0, st>>>(topk_length, p->s_q, p->topk, (uint32_t*)ws,
-                                                  (int32_t*)(ws + L.counters_off));
+    cudaLaunchConfig_t ocfg = {};
+    ocfg.gridDim = dim3(1);
+    ocfg.blockDim = dim3(ORDER_THREADS);
+    ocfg.stream = st;
+    cudaLaunchAttribute oattr[1];
+    oattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    oattr[0].val.programmaticStreamSerializationAllowed = 1;
+    ocfg.attrs = oattr;
+    ocfg.numAttrs = (p->flags & DSA_FLAG_AFTER_PRODUCER) ? 1 : 0;
+    if (cudaLaunchKernelEx(&ocfg, dsa_order_kernel, topk_length, p->s_q, p->topk, (uint32_t*)ws,
+                           (int32_t*)(ws + L.counters_off)) != cudaSuccess)
+      return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   } else {
     // header and the split arrival counters

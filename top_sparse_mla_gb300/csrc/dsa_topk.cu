@@ -84,6 +84,9 @@ __global__ void __launch_bounds__(THREADS, 4) topk_kernel(const uint16_t* __rest
   __shared__ int s_hist[256];
   __shared__ int s_wsum[WARPS];
   __shared__ int s_sel[2];
+  // a dependent launched with programmatic serialization (the attention with
+  // DSA_FLAG_AFTER_PRODUCER) may start now; it waits for this kernel before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const long long t = blockIdx.x;
   int L = n;
@@ -240,6 +243,9 @@ __global__ void __launch_bounds__(NT, MINB) topk_reg_kernel(const uint16_t* __re
   __shared__ int s_hist[2][256];
   __shared__ int s_wsum[NWARP];
   __shared__ int s_sel[4];
+  // a dependent launched with programmatic serialization (the attention with
+  // DSA_FLAG_AFTER_PRODUCER) may start now; it waits for this kernel before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const long long t = blockIdx.x;
   int L = n;

@@ -33,6 +33,7 @@ DSA_TOPK_MAX_K = 2048
 DSA_ROW_BYTES = 656
 DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 DSA_KV_FLAG_CHECK_SLOTS = 1
+DSA_FLAG_AFTER_PRODUCER = 4
 DSA_STATUS_SLOT_OUT_OF_RANGE = 4
 
 EXPORTED = (
