@@ -10,6 +10,8 @@ compared here):
 - "single": q~ = fp16 of q * w (roped), each latent value fp16(fp16(code) * fp16(scale)),
   P = fp16 of the softmax numerators, and the row sum over the fp16 P.  This is the
   plain fp16 tensor-core design.
+- "fp8q": the split design with the latent part of q~ quantised to E4M3 (one scale per
+  head, its largest magnitude mapped to 448), the operand an FP8 x FP8 QK^T would take.
 - "split": the fused kernel's design.  q~ = hi + lo (two fp16 parts of the fp32 value,
   after a per-head power-of-two prescale); the E4M3 codes enter unscaled (exact in fp16)
   and each 128-dim block's fp32 scale multiplies that block's partial score; PV takes,
@@ -50,7 +52,7 @@ def _rows(rows: np.ndarray):
 
 
 def token_output(design: str, q_bits, norm_w_bits, index_row, topk_length, pos, kv_swa, kv_cmp, p) -> np.ndarray:
-    """Pre-cast output [h, 512] of one token under `design` ("single" or "split")."""
+    """Pre-cast output [h, 512] of one token under `design` ("single", "split" or "fp8q")."""
     x = codecs.bf16_decode(q_bits)
     h = x.shape[0]
     cols = valid_columns(index_row, topk_length)
@@ -68,6 +70,13 @@ def token_output(design: str, q_bits, norm_w_bits, index_row, topk_length, pos, 
         amax = np.max(np.abs(x * codecs.bf16_decode(norm_w_bits)), axis=1, keepdims=True)
         k2 = np.where(amax > 0, 13.0 - np.floor(np.log2(np.where(amax > 0, amax, 1.0))), 0.0)
         qs = hi_lo(qt * np.exp2(k2)) * np.exp2(-k2)
+        if design == "fp8q":
+            # the latent part of q~ as E4M3 with a per-head scale (max |q~| maps to 448)
+            lat = qt[:, :D_LATENT]
+            qsc = np.max(np.abs(lat), axis=1, keepdims=True) / 448.0
+            qsc = np.where(qsc > 0, qsc, 1.0)
+            qs = qs.copy()
+            qs[:, :D_LATENT] = codecs.e4m3_decode(codecs.e4m3_encode(lat / qsc)) * qsc
         s = qs[:, D_LATENT:] @ f16(rope).T
         for b in range(D_LATENT // SCALE_GROUP):
             blk = slice(SCALE_GROUP * b, SCALE_GROUP * (b + 1))
