@@ -53,8 +53,17 @@ def spec_roofline_s(w) -> float:
 
 def algorithmic_bytes(w) -> int:
     """Bytes the path must move at least once: the valid gathered rows, q, the outputs,
-    the index row, the length and the position of every token."""
+    the index row, the length and the position of every token.  On the nvfp4_ds_mla
+    cache the rows are 528 bytes (window columns) and 288 bytes (compressed columns)
+    and q has 512 dims."""
     from top_sparse_mla_gb300 import workloads as W
+    if w.kv_format == 1:
+        cols = np.arange(w.topk)[None, :]
+        live = (cols < w.topk_length[:, None]) & (w.indices >= 0)
+        n_swa = int(live[:, :w.n_swa_cols].sum())
+        n_cmp = int(live[:, w.n_swa_cols:].sum())
+        per_tok = w.h_q * 512 * 2 + w.h_q * 512 + w.h_q * 16 + w.topk * 4 + 8
+        return n_swa * 528 + n_cmp * 288 + w.s_q * per_tok
     n_valid = int(W.n_valid_rows(w).sum())
     per_tok = w.h_q * 576 * 2 + w.h_q * 512 + w.h_q * 16 + w.topk * 4 + 8
     return n_valid * 656 + w.s_q * per_tok
@@ -62,7 +71,8 @@ def algorithmic_bytes(w) -> int:
 
 def algorithmic_flops(w) -> int:
     from top_sparse_mla_gb300 import workloads as W
-    return int(W.n_valid_rows(w).sum()) * (2 * w.h_q * 576 + 2 * w.h_q * 512)
+    d_qk = 512 if w.kv_format == 1 else 576
+    return int(W.n_valid_rows(w).sum()) * (2 * w.h_q * d_qk + 2 * w.h_q * 512)
 
 
 def kernels_per_call(params, num_sms: int = 0) -> int:
@@ -402,7 +412,7 @@ def run_native(args):
 
     per_config = {}
     if not args.skip_sweep and world == 1:
-        for name in ("decode1", "decode64", "decode1024", "prefill2123"):
+        for name in ("decode1", "decode64", "decode1024", "prefill2123", "decode1024_nvfp4"):
             wc = W.make(name) if name != args.workload else w
             ic = api.upload(wc, "cuda") if name != args.workload else inp
             oc = api.allocate_outputs(ic)

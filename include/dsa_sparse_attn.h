@@ -31,7 +31,8 @@
  *   positions   int32 [s_q]
  *   norm_w      bf16  [576]                              16-byte aligned
  *   out_fp8     uint8 [s_q, h_q, 512] E4M3 codes          16-byte aligned
- *   out_sf      uint8 [s_q, h_q, 16]  UE8M0 codes
+ *   out_sf      uint8 [s_q, h_q, 16]  UE8M0 codes (or, with DSA_FLAG_SF_SWIZZLED, the
+ *               same codes in the 128x4-tile layout described at that flag)
  *   out_precast fp32  [s_q, h_q, 512] (debug entry only; may be NULL) 16-byte aligned
  *   lse         fp32  [s_q, h_q] natural-log sum-exp of the scaled scores, -inf for
  *               a token with no valid column (debug entry only; may be NULL)
@@ -95,6 +96,21 @@ extern "C" {
  * first, which orders the call after the producer as usual; the flag then changes
  * nothing. */
 #define DSA_FLAG_AFTER_PRODUCER 4u
+/* Write out_sf in FlashInfer's 128x4 swizzled scale-factor layout, the one an MXFP8
+ * GEMM reading the output as an [s_q, 512 h_q] matrix takes ("[DSV4.1] Combine DSpark
+ * decode and prefill kernel optimizations", SGLang PR #39370, the mHC MXFP8 epilogue
+ * paragraph, names the layout; the byte order below is this library's reading of it).
+ * The scale matrix has M = s_q rows (tokens) and K = 16 h_q columns (column
+ * k = 16 h + b for head h and 32-dim block b).  It is stored as 128 x 4 tiles of 512
+ * bytes, tiles in row-major order (ceil(s_q / 128) tile rows of 4 h_q tiles); inside a
+ * tile, entry (m, k) is at byte (m % 32) * 16 + ((m / 32) % 4) * 4 + (k % 4).  So the
+ * byte offset of (m, k) is
+ *     ((m / 128) * 4 h_q + k / 4) * 512 + (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4,
+ * and out_sf must hold DSA_SF_SWIZZLED_BYTES(s_q, h_q) bytes.  The bytes of rows
+ * m >= s_q (the last tile row's padding) are not written.  The codes themselves, and
+ * every other output, are those of the row-major layout. */
+#define DSA_FLAG_SF_SWIZZLED 8u
+#define DSA_SF_SWIZZLED_BYTES(s_q, h_q) ((((size_t)(s_q) + 127) / 128) * 128 * 16 * (size_t)(h_q))
 
 #define DSA_STATUS_INDEX_OUT_OF_RANGE 1u /* an index was >= its pool size (with the flag) */
 #define DSA_STATUS_WAIT_TIMEOUT 2u       /* an on-chip pipeline wait gave up; output invalid */
@@ -104,6 +120,32 @@ extern "C" {
 #define DSA_MAX_TOPK 2048
 #define DSA_ORDER_MAX_TOKENS 65536 /* above this the queue takes tokens in index order */
 #define DSA_ROW_BYTES 656
+
+/* Cache formats (dsa_params.kv_format).
+ *
+ * DSA_KV_FP8_DS_MLA: the layout described at the top of this file (576-dim keys, q and
+ * norm_w of 576, 656-byte rows in both pools).
+ *
+ * DSA_KV_NVFP4_DS_MLA: the V4.1 cache that "Deepseek V41 Attention MegaKernel" (vLLM PR
+ * #56344, Purpose) adds as nvfp4_ds_mla, "V4.1 fp8 528 B SWA + V4.1 fp4 288 B
+ * compressed".  The page gives the two row sizes only; the byte layout below is this
+ * library's reading.  Keys are 512 dims with the 64 rotary dims inside (dims 448..511,
+ * stored already rotated), and v = k: the 512 output dims are the keys' dims, which is
+ * why the output's dims 448..511 get the inverse RoPE.  So q and norm_w have 512 dims
+ * (q RMSNorm over the 512, RoPE on q dims 448..511 with the same pair convention),
+ * s_j = softmax_scale * q~ . k_j (softmax_scale is still the caller's, e.g.
+ * 1/sqrt(512)), and steps 5-7 are unchanged.
+ *   kv_swa row, 528 bytes: 512 E4M3 values | 4 little-endian fp32 scales, scale g
+ *     for dims [128g, 128g + 128).
+ *   kv_cmp row, 288 bytes (NVFP4): 512 E2M1 values, two per byte (dim 2i in the low
+ *     nibble of byte i) | 32 E4M3 scales, scale i for dims [16i, 16i + 16).  The value
+ *     of dim d is e2m1 * e4m3 scale * cmp_scale.
+ * Rows are 16-byte aligned (528 = 33 * 16, 288 = 18 * 16). */
+#define DSA_KV_FP8_DS_MLA 0
+#define DSA_KV_NVFP4_DS_MLA 1
+#define DSA_NVFP4_QK_DIMS 512
+#define DSA_NVFP4_SWA_ROW_BYTES 528
+#define DSA_NVFP4_CMP_ROW_BYTES 288
 #define DSA_NOALLOC_SCRATCH_BYTES (24u << 20) /* built-in scratch of the no-alloc entry */
 
 typedef struct dsa_params {
@@ -117,10 +159,13 @@ typedef struct dsa_params {
   float rope_base;      /* e.g. 10000 */
   float rms_eps;        /* e.g. 1e-6 */
   uint32_t flags;       /* DSA_FLAG_* */
+  int32_t kv_format;    /* DSA_KV_FP8_DS_MLA or DSA_KV_NVFP4_DS_MLA (see below) */
+  float cmp_scale;      /* DSA_KV_NVFP4_DS_MLA: fp32 scale of every kv_cmp value, finite */
 } dsa_params;
 
 /* Fill `p` with the defaults above for the given shape (softmax_scale 1/sqrt(576),
- * rope_base 10000, rms_eps 1e-6, flags 0).  Returns DSA_OK or DSA_ERR_INVALID_ARG. */
+ * rope_base 10000, rms_eps 1e-6, flags 0, kv_format DSA_KV_FP8_DS_MLA, cmp_scale 1).
+ * Returns DSA_OK or DSA_ERR_INVALID_ARG. */
 int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32_t n_swa_cols,
                     int64_t n_swa_rows, int64_t n_cmp_rows);
 

@@ -21,9 +21,11 @@ Modules:
                  and Validation)
   kv_insert   -- the KV-cache insert: norm, RoPE and fp8_ds_mla quantisation of new rows
                  (vLLM PR #64364, "The changes and what each bought", Attention)
+  nvfp4       -- the same attention on the nvfp4_ds_mla (V4.1) cache: 512-dim keys with
+                 the rotary dims inside, fp8 and fp4 rows (vLLM PR #56344, Purpose)
 """
 
-from . import codecs, sparse_mla, brute, topk, kv_insert  # noqa: F401
+from . import codecs, sparse_mla, brute, topk, kv_insert, nvfp4  # noqa: F401
 from .sparse_mla import (  # noqa: F401
     OracleParams,
     decode_kv_rows,

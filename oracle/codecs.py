@@ -178,3 +178,28 @@ def mxfp8_quantize(x, block: int = 32):
     codes = e4m3_encode(scaled).reshape(x.shape)
     sf = (e + 127).astype(np.uint8)
     return codes, sf
+
+
+def sf_swizzle_128x4(sf) -> np.ndarray:
+    """Scale codes [M, K] (K a multiple of 4) laid out in 128 x 4 tiles, as the bytes of
+    FlashInfer's 128x4 scale-factor swizzle; rows M..ceil(M/128)*128 - 1 are zero.
+
+    The page ("[DSV4.1] Combine DSpark decode and prefill kernel optimizations", SGLang
+    PR #39370, mHC MXFP8 epilogue paragraph) names the layout but prints no byte order;
+    the reading taken: tiles of 128 rows x 4 columns, 512 bytes each, in row-major tile
+    order; inside a tile, row m and column k sit at (m % 32) * 16 + (m // 32) * 4 + k,
+    so that the four 32-row quarters of the tile interleave at a 4-byte stride and a
+    row's four codes are adjacent.  Written out entry by entry from that description.
+    """
+    sf = np.asarray(sf, dtype=np.uint8)
+    M, K = sf.shape
+    assert K % 4 == 0
+    m_pad = -(-M // 128) * 128
+    out = np.zeros(m_pad * K, dtype=np.uint8)
+    tiles_per_row = K // 4
+    for m in range(M):
+        for k in range(K):
+            tile = (m // 128) * tiles_per_row + k // 4
+            r, c = m % 128, k % 4
+            out[tile * 512 + (r % 32) * 16 + (r // 32) * 4 + c] = sf[m, k]
+    return out

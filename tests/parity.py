@@ -54,10 +54,15 @@ def subset(w: Workload, tokens) -> Workload:
     tokens = np.asarray(tokens)
     return Workload(name=w.name + "_subset", q=w.q[tokens], norm_w=w.norm_w, kv_swa=w.kv_swa, kv_cmp=w.kv_cmp,
                     indices=w.indices[tokens], topk_length=w.topk_length[tokens], positions=w.positions[tokens],
-                    n_swa_cols=w.n_swa_cols, seed=w.seed)
+                    n_swa_cols=w.n_swa_cols, seed=w.seed, kv_format=w.kv_format, cmp_scale=w.cmp_scale,
+                    softmax_scale=w.softmax_scale)
 
 
 def run_oracle(w: Workload):
+    if w.kv_format == 1:   # nvfp4_ds_mla: the softmax scale as the kernel receives it (fp32)
+        p = oracle.OracleParams(n_swa_cols=w.n_swa_cols, softmax_scale=float(np.float32(w.softmax_scale)))
+        return oracle.nvfp4.sparse_mla_forward(w.q, w.kv_swa, w.kv_cmp, w.indices, w.topk_length, w.positions,
+                                               w.norm_w, p, cmp_scale=w.cmp_scale)
     return oracle.sparse_mla_forward(w.q, w.kv_swa, w.kv_cmp, w.indices, w.topk_length, w.positions, w.norm_w,
                                      oracle.OracleParams(n_swa_cols=w.n_swa_cols))
 

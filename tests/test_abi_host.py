@@ -59,9 +59,9 @@ def test_flag_mask(lib):
     # the defined flags pass the argument check (num_splits returns 0 on a bad argument)
     p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096,
                                flags=native.DSA_FLAG_CHECK_INDICES | native.DSA_FLAG_TEST_WAIT_TIMEOUT
-                               | native.DSA_FLAG_AFTER_PRODUCER)
+                               | native.DSA_FLAG_AFTER_PRODUCER | native.DSA_FLAG_SF_SWIZZLED)
     assert native.dsa_sparse_attn_num_splits(p, 152) == 8
-    for bad in (8, 16, 1 << 31):
+    for bad in (16, 32, 1 << 31):
         p.flags = bad
         assert native.dsa_sparse_attn_num_splits(p, 152) == 0
 
@@ -190,7 +190,7 @@ def test_argument_validation_happens_before_any_gpu_work(lib):
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
     p = native.dsa_params_init(2, 64, 640, 128, 1 << 31, 2000)
     assert _call(lib, p) == native.DSA_ERR_UNSUPPORTED_SHAPE
-    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, flags=8)
+    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, flags=16)
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
     p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, softmax_scale=float("nan"))
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
@@ -200,3 +200,21 @@ def test_argument_validation_happens_before_any_gpu_work(lib):
     # swa-only / cmp-only shapes do not need the other pool
     p = native.dsa_params_init(2, 64, 640, 640, 1000, 0)
     assert _call(lib, p, kv_cmp=None, q=8) == native.DSA_ERR_INVALID_ARG   # fails on q, not on the missing pool
+
+
+def test_cache_format_arguments(lib):
+    # the two formats pass the argument check; an unknown format or a non-finite
+    # compressed-pool scale does not (num_splits returns 0 on a bad argument)
+    p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096)
+    assert p.kv_format == native.DSA_KV_FP8_DS_MLA and p.cmp_scale == 1.0
+    p.kv_format = native.DSA_KV_NVFP4_DS_MLA
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 8
+    for fmt in (2, -1):
+        p.kv_format = fmt
+        assert native.dsa_sparse_attn_num_splits(p, 152) == 0
+    p.kv_format = native.DSA_KV_NVFP4_DS_MLA
+    for bad in (float("nan"), float("inf"), float("-inf")):
+        p.cmp_scale = bad
+        assert native.dsa_sparse_attn_num_splits(p, 152) == 0
+    p.cmp_scale = 0.0
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 8

@@ -331,3 +331,42 @@ def test_bf16_encode_matches_torch_rounding():
     assert C.bf16_encode(np.array([np.nan]))[0] == 0x7FC0
     # ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 and goes to the even 1
     assert C.bf16_encode(np.array([1.00390625]))[0] == 0x3F80
+
+
+def test_sf_swizzle_128x4_hand_worked_offsets():
+    # A 130 x 8 scale matrix: two tile rows (the second one padded) of two 128 x 4 tiles.
+    # Offsets worked by hand from the layout's description: tiles of 512 bytes in
+    # row-major tile order; inside a tile, row r and column c at (r % 32) * 16 +
+    # (r // 32) * 4 + c.
+    from oracle import codecs as C
+    M, K = 130, 8
+    sf = np.zeros((M, K), dtype=np.uint8)
+    marks = {  # (m, k): expected byte offset
+        (0, 0): 0, (0, 3): 3, (0, 4): 512, (1, 0): 16, (31, 0): 496, (32, 0): 4, (33, 1): 16 + 4 + 1,
+        (64, 2): 8 + 2, (96, 0): 12, (127, 3): 496 + 12 + 3, (127, 7): 512 + 511, (128, 0): 1024,
+        (129, 7): 1536 + 16 + 3,
+    }
+    for i, (m, k) in enumerate(marks):
+        sf[m, k] = 10 + i
+    out = C.sf_swizzle_128x4(sf)
+    assert out.shape == (256 * K,)          # rows padded to a multiple of 128
+    for i, ((m, k), off) in enumerate(marks.items()):
+        assert out[off] == 10 + i, (m, k, off)
+    assert int(np.count_nonzero(out)) == len(marks)
+
+
+def test_sf_swizzle_128x4_is_a_permutation():
+    # with M a multiple of 128 every byte is written exactly once
+    from oracle import codecs as C
+    rng = np.random.default_rng(5)
+    for M, K in ((128, 4), (256, 16), (384, 64)):
+        sf = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+        out = C.sf_swizzle_128x4(sf)
+        assert out.size == sf.size
+        assert np.array_equal(np.sort(out), np.sort(sf.ravel()))
+        # each 512-byte tile holds exactly the codes of its 128 x 4 block
+        for mt in range(M // 128):
+            for kt in range(K // 4):
+                tile = out[(mt * (K // 4) + kt) * 512:(mt * (K // 4) + kt + 1) * 512]
+                block = sf[128 * mt:128 * (mt + 1), 4 * kt:4 * (kt + 1)]
+                assert np.array_equal(np.sort(tile), np.sort(block.ravel()))

@@ -17,20 +17,20 @@ from .workloads import Workload
 
 @dataclass
 class DeviceInputs:
-    q: torch.Tensor            # uint16 view of bf16 [s_q, h_q, 576]
-    kv_swa: torch.Tensor       # uint8 [n_swa_rows, 656]
-    kv_cmp: torch.Tensor       # uint8 [n_cmp_rows, 656]
+    q: torch.Tensor            # uint16 view of bf16 [s_q, h_q, 576] (512: nvfp4_ds_mla)
+    kv_swa: torch.Tensor       # uint8 [n_swa_rows, 656] (528: nvfp4_ds_mla)
+    kv_cmp: torch.Tensor       # uint8 [n_cmp_rows, 656] (288: nvfp4_ds_mla)
     indices: torch.Tensor      # int32 [s_q, topk]
     topk_length: torch.Tensor  # int32 [s_q]
     positions: torch.Tensor    # int32 [s_q]
-    norm_w: torch.Tensor       # uint16 view of bf16 [576]
+    norm_w: torch.Tensor       # uint16 view of bf16 [576] (512: nvfp4_ds_mla)
     params: native.DsaParams
 
 
 @dataclass
 class DeviceOutputs:
     out_fp8: torch.Tensor      # uint8 [s_q, h_q, 512]
-    out_sf: torch.Tensor       # uint8 [s_q, h_q, 16]
+    out_sf: torch.Tensor       # uint8 [s_q, h_q, 16] (flat 128x4 tiles with DSA_FLAG_SF_SWIZZLED)
     out_precast: torch.Tensor | None
     lse: torch.Tensor | None
     workspace: torch.Tensor
@@ -47,6 +47,9 @@ def upload(w: Workload, device="cuda", flags: int = 0) -> DeviceInputs:
     # uint16 bit patterns travel as int16 (torch has no general uint16 ops)
     p = native.dsa_params_init(w.s_q, w.h_q, w.topk, w.n_swa_cols, w.kv_swa.shape[0], w.kv_cmp.shape[0])
     p.flags = flags
+    p.kv_format = w.kv_format
+    p.cmp_scale = w.cmp_scale
+    p.softmax_scale = w.softmax_scale
     return DeviceInputs(
         q=_dev(w.q.view(np.int16), device, None),
         kv_swa=_dev(w.kv_swa, device, None),
@@ -67,7 +70,10 @@ def allocate_outputs(inp: DeviceInputs, debug: bool = False) -> DeviceOutputs:
         raise native.DsaError(native.DSA_ERR_INVALID_ARG, "dsa_sparse_attn_workspace_size")
     return DeviceOutputs(
         out_fp8=torch.empty((p.s_q, p.h_q, 512), dtype=torch.uint8, device=dev),
-        out_sf=torch.empty((p.s_q, p.h_q, 16), dtype=torch.uint8, device=dev),
+        # row-major [s_q, h_q, 16], or the flat 128x4-tile layout (DSA_FLAG_SF_SWIZZLED)
+        out_sf=(torch.empty(native.sf_swizzled_bytes(p.s_q, p.h_q), dtype=torch.uint8, device=dev)
+                if p.flags & native.DSA_FLAG_SF_SWIZZLED else
+                torch.empty((p.s_q, p.h_q, 16), dtype=torch.uint8, device=dev)),
         out_precast=torch.empty((p.s_q, p.h_q, 512), dtype=torch.float32, device=dev) if debug else None,
         lse=torch.empty((p.s_q, p.h_q), dtype=torch.float32, device=dev) if debug else None,
         workspace=torch.empty(((ws_bytes + 255) // 256) * 256, dtype=torch.uint8, device=dev),

@@ -154,6 +154,8 @@ struct KParams {
   float score_scale_log2;   // softmax_scale * log2(e)
   float rms_eps;
   uint32_t flags;
+  // nvfp4_ds_mla (the kernel's V41 instantiation): every kv_cmp value times cmp_scale
+  float cmp_scale;
   int n_splits;
   int n_halves;             // 1 when h_q <= 32, else 2
   int n_items;
@@ -221,9 +223,36 @@ struct Group {
   }
 };
 
+// The kernel is compiled once per cache format (template argument V41: the
+// nvfp4_ds_mla format), so that the format costs no run-time test in the hot loops.
+template <bool V41>
+struct Fmt {
+  static constexpr int d_q = V41 ? DSA_NVFP4_QK_DIMS : D_QK;              // q / norm_w dims
+  static constexpr uint32_t swa_row = V41 ? DSA_NVFP4_SWA_ROW_BYTES : ROW_BYTES;
+  static constexpr uint32_t cmp_row = V41 ? DSA_NVFP4_CMP_ROW_BYTES : ROW_BYTES;
+};
+template <bool V41>
 DSA_DEV const uint8_t* row_ptr(const KParams& P, uint32_t e) {
-  const uint8_t* base = (e & 0x80000000u) ? P.kv_cmp : P.kv_swa;
-  return base + (size_t)(e & 0x7FFFFFFFu) * ROW_BYTES;
+  const bool cmp = (e & 0x80000000u) != 0;
+  return (cmp ? P.kv_cmp : P.kv_swa) + (size_t)(e & 0x7FFFFFFFu) * (cmp ? Fmt<V41>::cmp_row : Fmt<V41>::swa_row);
+}
+template <bool V41>
+DSA_DEV uint32_t row_bytes(uint32_t e) {
+  return (e & 0x80000000u) ? Fmt<V41>::cmp_row : Fmt<V41>::swa_row;
+}
+// An nvfp4_ds_mla compressed row: its values carry 16-dim E4M3 scales inside the row
+// (folded into the fp16 codes by the dequant warps), and one fp32 scale for the pool.
+template <bool V41>
+DSA_DEV bool fp4_row(uint32_t e) { return V41 && (e & 0x80000000u) != 0; }
+// The four fp32 block scales of a row (one per 128 dims) as raw bits: bytes 512..527 of
+// an fp8 row; cmp_scale four times for an fp4 row.
+template <bool V41>
+DSA_DEV uint4 row_scales(const KParams& P, uint32_t e) {
+  if (fp4_row<V41>(e)) {
+    const uint32_t g = __float_as_uint(P.cmp_scale);
+    return make_uint4(g, g, g, g);
+  }
+  return ldg_nc(row_ptr<V41>(P, e) + D_LAT);
 }
 DSA_DEV const uint32_t* item_list(const KParams& P, int b) {
   return P.lists + ((size_t)blockIdx.x * NB + b) * DSA_MAX_TOPK;
@@ -234,6 +263,28 @@ DSA_DEV const float* item_ref(const Ctx& c, int b) {
 }
 DSA_DEV const float* item_iref(const Ctx& c, int b) {
   return reinterpret_cast<const float*>(c.sm + SM_ITEM) + 16 * b + IT_IREF;
+}
+
+// Output pointers of the MXFP8 finish (passed by value to the out-of-line callers).
+struct OutPtrs {
+  uint8_t* fp8;
+  uint8_t* sf;
+  float* precast;
+  int h_q;
+  int sf_swizzled;   // DSA_FLAG_SF_SWIZZLED
+};
+DSA_DEV OutPtrs out_ptrs(const KParams& P) {
+  return OutPtrs{P.out_fp8, P.out_sf, P.out_precast, P.h_q, (P.flags & DSA_FLAG_SF_SWIZZLED) ? 1 : 0};
+}
+// Byte offset of the scale code of (token t, head h, 32-dim block blk) in out_sf.  Row
+// major: [s_q, h_q, 16].  Swizzled: the [s_q, 16 h_q] scale matrix (m = t, k = 16 h +
+// blk) in 128 x 4 tiles of 512 bytes, tiles row-major; inside a tile, (m % 32, m / 32 %
+// 4, k % 4) with strides 16, 4, 1 (FlashInfer's 128x4 swizzle, named on "[DSV4.1]
+// Combine DSpark decode and prefill kernel optimizations", mHC MXFP8 epilogue).
+DSA_DEV size_t sf_offset(const OutPtrs& O, int t, int h, int blk) {
+  if (!O.sf_swizzled) return ((size_t)t * O.h_q + h) * 16 + blk;
+  const int k = 16 * h + blk;
+  return ((size_t)(t >> 7) * (size_t)(4 * O.h_q) + (size_t)(k >> 2)) * 512 + (size_t)((t & 31) * 16 + ((t >> 5) & 3) * 4 + (k & 3));
 }
 
 // ================================================================== PREP
@@ -251,7 +302,8 @@ __device__ __noinline__ void write_empty_item(const KParams& P, int t, int half,
       for (int u = 0; u < 4; ++u) pc[4 * k + u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  for (int i = lane; i < nh * 16; i += 32) P.out_sf[((size_t)t * P.h_q + h0) * 16 + i] = 0;
+  const OutPtrs O = out_ptrs(P);
+  for (int i = lane; i < nh * 16; i += 32) P.out_sf[sf_offset(O, t, h0 + (i >> 4), i & 15)] = 0;
   if (P.out_lse && lane < nh) P.out_lse[(size_t)t * P.h_q + h0 + lane] = -INFINITY;
 }
 
@@ -262,6 +314,7 @@ DSA_DEV uint32_t redux_max_u32(uint32_t v) {
 }
 
 // Items, row lists, reference scales and rotary tables, ahead of the other roles.
+template <bool V41>
 DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   int* s_items = reinterpret_cast<int*>(c.sm + SM_ITEM);
   const bool split_path = P.n_splits > 1;
@@ -365,7 +418,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
     // |scale| of the item's rows, so that P_b = P * scale / reference stays below 2 P.
     float mx[4] = {0.f, 0.f, 0.f, 0.f};
     for (int i = lane; i < nrows; i += 32) {
-      const uint4 s = ldg_nc(row_ptr(P, __ldcg(list + row0 + i)) + D_LAT);
+      const uint4 s = row_scales<V41>(P, __ldcg(list + row0 + i));
       mx[0] = fmaxf(mx[0], fabsf(__uint_as_float(s.x)));
       mx[1] = fmaxf(mx[1], fabsf(__uint_as_float(s.y)));
       mx[2] = fmaxf(mx[2], fabsf(__uint_as_float(s.z)));
@@ -404,14 +457,6 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   }
 }
 
-// Output pointers of the MXFP8 finish (passed by value to the out-of-line callers).
-struct OutPtrs {
-  uint8_t* fp8;
-  uint8_t* sf;
-  float* precast;
-  int h_q;
-};
-
 // Finish 32 consecutive output dims of one head in one thread: inverse RoPE, optional
 // pre-cast store, MXFP8 (one 32-value block) and the stores.
 DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int d0, const float2* rope) {
@@ -446,7 +491,7 @@ DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int 
   uint4* dst = reinterpret_cast<uint4*>(O.fp8 + row * D_LAT + d0);
   dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
   dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-  O.sf[row * 16 + (d0 >> 5)] = (uint8_t)(E + 127);
+  O.sf[sf_offset(O, t, h, d0 >> 5)] = (uint8_t)(E + 127);
 }
 
 // Finish dim d of heads h0..h0+N-1, one head per register; the 32 lanes of the warp hold
@@ -489,7 +534,7 @@ DSA_DEV void finalize_lanes(const OutPtrs& O, float (&v)[N], int t, int h0, int 
     if (h0 + i + 1 < O.h_q) out[(size_t)(i + 1) * D_LAT] = (uint8_t)(q >> 8);
     sfw = lane == i ? (uint32_t)(e0 + 127) : (lane == i + 1 ? (uint32_t)(e1 + 127) : sfw);
   }
-  if (lane < N && h0 + lane < O.h_q) O.sf[(row0 + lane) * 16 + (d >> 5)] = (uint8_t)sfw;
+  if (lane < N && h0 + lane < O.h_q) O.sf[sf_offset(O, t, h0 + lane, d >> 5)] = (uint8_t)sfw;
 }
 
 // Epilogue of the 128-dim column block cidx of O^T by a warp on TMEM lane quarter q4
@@ -560,22 +605,26 @@ struct QArgs {
   float eps, c2;
 };
 
+template <bool V41>
 DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
+  constexpr int d_q = Fmt<V41>::d_q;         // 576 (rotary atom 8) or 512 (rotary atom 7)
   const int* info = item_info(c, b);
   const int hs = er >> 3, chn = er & 7;
   const int h = HH * info[IT_HALF] + hs;
   const bool hv = h < P.h_q;
-  const uint16_t* qh = P.q + ((size_t)info[IT_TOKEN] * P.h_q + (hv ? h : 0)) * D_QK + 8 * chn;
+  const uint16_t* qh = P.q + ((size_t)info[IT_TOKEN] * P.h_q + (hv ? h : 0)) * d_q + 8 * chn;
   const uint16_t* wp = P.norm_w + 8 * chn;
   const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
+  constexpr int na = d_q / 64;               // 64-dim atoms of q: 9, or 8
+  constexpr int ra = na - 1;                 // the rotary atom
   uint4 raw[9];
 #pragma unroll
-  for (int a = 0; a < 9; ++a) raw[a] = hv ? ldg_nc(qh + 64 * a) : make_uint4(0, 0, 0, 0);
+  for (int a = 0; a < 9; ++a) raw[a] = (hv && a < na) ? ldg_nc(qh + 64 * a) : make_uint4(0, 0, 0, 0);
   // pass 1: sum of squares of q, largest |q * w|
   float ss = 0.f, amax = 0.f;
 #pragma unroll
   for (int a = 0; a < 9; ++a) {
-    const uint4 wq = ldg_nc(wp + 64 * a);
+    const uint4 wq = a < na ? ldg_nc(wp + 64 * a) : make_uint4(0, 0, 0, 0);
     const uint32_t x4[4] = {raw[a].x, raw[a].y, raw[a].z, raw[a].w};
     const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
@@ -596,9 +645,15 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
   int k = ea == 0 ? 0 : 140 - ea;
   k = k < -100 ? -100 : (k > 100 ? 100 : k);
   const float sk = __uint_as_float((uint32_t)(127 + k) << 23);     // 2^k, exact
-  // pass 2: the hi / lo operand rows (unrolled: raw[] stays in registers)
+  // pass 2: the hi / lo operand rows (unrolled: raw[] stays in registers); with 512-dim
+  // q the ninth atom stays unwritten (its QK^T partial is not run) but is announced all
+  // the same, so that QRDY keeps one phase per item
 #pragma unroll
   for (int a = 0; a < 9; ++a) {
+    if (a >= na) {
+      arrive_w(c, B_QRDY + 4);
+      continue;
+    }
     const uint4 wq = ldg_nc(wp + 64 * a);
     const uint32_t x4[4] = {raw[a].x, raw[a].y, raw[a].z, raw[a].w};
     const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
@@ -608,7 +663,7 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
       x[2 * e] = __uint_as_float(x4[e] << 16) * __uint_as_float(w4[e] << 16) * sk;
       x[2 * e + 1] = __uint_as_float(x4[e] & 0xFFFF0000u) * __uint_as_float(w4[e] & 0xFFFF0000u) * sk;
     }
-    if (a == 8) {   // dims 512..575: the rotary pairs 4 chn + e
+    if (a == ra) {   // dims 512..575 (or 448..511): the rotary pairs 4 chn + e
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 cs = rope[4 * chn + e];
@@ -630,7 +685,7 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
     }
   }
   float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 32 * b;
-  if (chn == 0) s_inv[hs] = hv ? rsqrtf(ss * (1.0f / D_QK) + P.eps) * P.c2 * __uint_as_float((uint32_t)(127 - k) << 23)
+  if (chn == 0) s_inv[hs] = hv ? rsqrtf(ss * (1.0f / d_q) + P.eps) * P.c2 * __uint_as_float((uint32_t)(127 - k) << 23)
                                : 0.f;
   arrive_w(c, B_QSTAT + b);
 }
@@ -658,12 +713,26 @@ DSA_DEV void dq_load_rows(const uint32_t* list, int tt, int nrows, int w, int su
   }
 }
 
+// The raw bytes of dims 128 cidx + 16 ch .. + 15 of rows R: 16 E4M3 codes of an fp8 row;
+// of an fp4 row, 16 E2M1 values (x, y) and their E4M3 scale (z).
+template <bool V41>
 DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const DqRows& R, int ch) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    dst[k] = R.e[k] != NO_ROW ? ldg_nc(row_ptr(P, R.e[k]) + 128 * cidx + 16 * ch) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t e = R.e[k];
+    if (e == NO_ROW) {
+      dst[k] = make_uint4(0, 0, 0, 0);
+    } else if (fp4_row<V41>(e)) {
+      const uint8_t* rp = row_ptr<V41>(P, e);
+      const uint2 v = ldg_nc_v2(rp + 64 * cidx + 8 * ch);
+      dst[k] = make_uint4(v.x, v.y, ldg_nc_u8(rp + 256 + 8 * cidx + ch), 0);
+    } else {
+      dst[k] = ldg_nc(row_ptr<V41>(P, e) + 128 * cidx + 16 * ch);
+    }
+  }
 }
 
+template <bool V41>
 DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int lane) {
   const int sub = lane >> 3, ch = lane & 7;
   const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
@@ -685,7 +754,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
     if (!wait_bar_w(c, B_ODONE, pend_nq & 1)) return false;
     if (!wait_bar_w(c, B_LREADY, pend_nq & 1)) return false;
     tc_fence_after();
-    const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
+    const OutPtrs O = out_ptrs(P);
     const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * pbf;
     const int* pinfo = item_info(c, pbf);
     const int cidx = 1 + (w >> 2);
@@ -706,10 +775,10 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
         if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
-        build_q(qa, c, b, 32 * w + lane);
+        build_q<V41>(qa, c, b, 32 * w + lane);
         dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, cur);
-        dq_load_chunk(P, raw[0], qk_chunk(0), cur, ch);
-        dq_load_chunk(P, raw[1], qk_chunk(1), cur, ch);
+        dq_load_chunk<V41>(P, raw[0], qk_chunk(0), cur, ch);
+        dq_load_chunk<V41>(P, raw[1], qk_chunk(1), cur, ch);
         return 1;
       }
       arrive_w(c, B_QSTAT + b);   // no q~: the phase still follows the buffer's uses
@@ -752,9 +821,12 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
           // lanes of the second 64-dim atom (ch >= 4) store their upper eight dims first:
           // the eight lanes of a row then hit eight distinct 16-byte bank groups
           const uint4 rw = raw[pos & 1][k];
-          const uint4 rr = ch >= 4 ? make_uint4(rw.z, rw.w, rw.x, rw.y) : rw;
           uint32_t o[8];
-          codes16_to_f16(rr, o);
+          if (cur.e[k] != NO_ROW && fp4_row<V41>(cur.e[k])) {
+            fp4x16_to_f16(ch >= 4 ? rw.y : rw.x, ch >= 4 ? rw.x : rw.y, rw.z, o);
+          } else {
+            codes16_to_f16(ch >= 4 ? make_uint4(rw.z, rw.w, rw.x, rw.y) : rw, o);
+          }
           const uint32_t row = (uint32_t)(16 * w + 4 * k + sub);
           const uint32_t rsw = row & 7;
           const uint32_t rb = cbase + (row >> 3) * 1024 + rsw * 128;
@@ -763,17 +835,24 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
         }
         fence_async_smem();
         arrive_w(c, B_VFULL + cidx);
-        if (pos == 0 && pf && ch < 6) {
-          // the six 128-byte lines of each next row, one line per lane
+        if (pos == 0 && pf) {
+          // the 128-byte lines of each next row (at most six), one line per lane: lane ch
+          // takes the line of byte min(128 ch, last byte), for the lines a row starting
+          // anywhere on a 16-byte boundary can touch
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (nxt.e[k] != NO_ROW) prefetch_line_l2(row_ptr(P, nxt.e[k]) + 128 * ch);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t e = nxt.e[k];
+            if (e == NO_ROW) continue;
+            const uint32_t rb = row_bytes<V41>(e);
+            if ((uint32_t)ch < (rb + 112 + 127) / 128)
+              prefetch_line_l2(row_ptr<V41>(P, e) + min(128u * (uint32_t)ch, rb - 1));
+          }
         }
         // the chunk two positions ahead
         if (pos < 2) {
-          dq_load_chunk(P, raw[pos & 1], qk_chunk(pos + 2), cur, ch);
+          dq_load_chunk<V41>(P, raw[pos & 1], qk_chunk(pos + 2), cur, ch);
         } else if (more) {
-          dq_load_chunk(P, raw[pos & 1], qk_chunk(pos - 2), nxt, ch);
+          dq_load_chunk<V41>(P, raw[pos & 1], qk_chunk(pos - 2), nxt, ch);
         }
       }
       if (more) cur = nxt;
@@ -817,6 +896,7 @@ DSA_DEV void commit(uint32_t bar_addr) {
   __syncwarp();
 }
 
+template <bool V41>
 DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   constexpr uint32_t IDESC_QK = idesc_f16(128, NQ, 0, 0);
   constexpr uint32_t IDESC_PV = idesc_f16(128, NQ, 1, 1);
@@ -856,7 +936,7 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
         commit(bar(c, B_SFULL + sbf));
         ++np;
       }
-      {
+      if constexpr (!V41) {   // (nvfp4_ds_mla keys hold their rotary dims inside the latent chunks)
         const uint32_t sbf = np % NSB;
         const uint32_t kb = g & 1;
         if (!wait_bar_w(c, B_SFREE + sbf, ((np / NSB) & 1) ^ 1)) return;
@@ -902,10 +982,19 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
 // tile: the rotary part of its keys (bf16 -> fp16 into TMEM, the A operand of the rope
 // partial; each group converts half of the 64 dims) and the row's four block scales,
 // read one tile ahead of their use.
+template <bool V41>
 DSA_DEV void sx_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
                      int nrows, int r, int gq, uint32_t gk, float (&scl)[4]) {
   const bool valid = tt * TILE + r < nrows;
-  const uint8_t* src = valid ? row_ptr(P, __ldcg(list + tt * TILE + r)) + D_LAT : nullptr;
+  if constexpr (V41) {   // no separate rotary keys: the four block scales only
+    const uint4 sv = valid ? row_scales<V41>(P, __ldcg(list + tt * TILE + r)) : make_uint4(0, 0, 0, 0);
+    scl[0] = __uint_as_float(sv.x);
+    scl[1] = __uint_as_float(sv.y);
+    scl[2] = __uint_as_float(sv.z);
+    scl[3] = __uint_as_float(sv.w);
+    return;
+  }
+  const uint8_t* src = valid ? row_ptr<V41>(P, __ldcg(list + tt * TILE + r)) + D_LAT : nullptr;
   uint4 raw[5];
   raw[0] = valid ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -948,6 +1037,7 @@ DSA_DEV void store_pb(uint32_t base, int r, int gq, const float (&p)[16], float 
   }
 }
 
+template <bool V41>
 DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int q4, int lane) {
   const int r = q4 * 32 + lane;
   const int hb = 16 * gq;                       // the group's first head within the item
@@ -988,7 +1078,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
-        sx_rope(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, gq, g, scl);
+        sx_rope<V41>(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, gq, g, scl);
         return c.misc[M_ABORT] ? -1 : 1;
       }
       if (is_split) {
@@ -1019,8 +1109,8 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         if (ni[IT_ITEM] >= 0 && ni[IT_T] > 0) {
           const int nh0 = HH * ni[IT_HALF];
           const int nh = (P.h_q - nh0) < HH ? (P.h_q - nh0) : HH;
-          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + ((size_t)ni[IT_TOKEN] * P.h_q + nh0) * D_QK);
-          for (int l = r; l < nh * 9; l += 128) prefetch_line_l2(qn + 128 * l);
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(P.q + ((size_t)ni[IT_TOKEN] * P.h_q + nh0) * Fmt<V41>::d_q);
+          for (int l = r; l < nh * (Fmt<V41>::d_q / 64); l += 128) prefetch_line_l2(qn + 128 * l);
         }
       }
     }
@@ -1039,8 +1129,9 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       float y[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) y[h] = 0.f;
+      constexpr int npart = V41 ? 4 : NPART;   // nvfp4_ds_mla: no rope partial
 #pragma unroll 1
-      for (int p = 0; p < NPART; ++p) {
+      for (int p = 0; p < npart; ++p) {
         const uint32_t sbf = np % NSB;
         if (!wait_bar_w(c, B_SFULL + sbf, (np / NSB) & 1)) return;
         tc_fence_after();
@@ -1132,7 +1223,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       }
       ++g;
       if (tt + 1 < T) {
-        sx_rope(P, c, tmem, tlane, list, tt + 1, nrows, r, gq, g, scl);
+        sx_rope<V41>(P, c, tmem, tlane, list, tt + 1, nrows, r, gq, g, scl);
         if (c.misc[M_ABORT]) return;
         continue;
       }
@@ -1156,7 +1247,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       // without splits column blocks 1 and 2 are finished by the dequant warps once 1/l
       // is out
       if (!is_split) arrive_w(c, B_LREADY);
-      const OutPtrs O{P.out_fp8, P.out_sf, P.out_precast, P.h_q};
+      const OutPtrs O = out_ptrs(P);
       const float2* rope = reinterpret_cast<const float2*>(c.sm + SM_ROPE) + 32 * b;
       float* part = is_split ? P.part_o + (((size_t)t * P.n_splits + split) * 64 + h0) * D_LAT : nullptr;
       const float* ref = item_ref(c, b);
@@ -1238,7 +1329,7 @@ DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int half, int 
         v[4 * k + 3] = fmaf(w0, f0[k].w, fmaf(w1, f1[k].w, v[4 * k + 3]));
       }
     }
-    finalize_block(OutPtrs{P.out_fp8, P.out_sf, P.out_precast, P.h_q}, v, t, h0 + hh, 32 * blk, rope);
+    finalize_block(out_ptrs(P), v, t, h0 + hh, 32 * blk, rope);
   }
 }
 
@@ -1311,6 +1402,7 @@ __global__ void __launch_bounds__(ORDER_THREADS, 1) dsa_order_kernel(const int32
   }
 }
 
+template <bool V41>
 __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
@@ -1368,13 +1460,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < W_SX) {
-    dq_role(P, c, tmem, warp, lane);
+    dq_role<V41>(P, c, tmem, warp, lane);
   } else if (warp < W_MMA) {
-    sx_role(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
+    sx_role<V41>(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
   } else if (warp == W_MMA) {
-    mma_role(P, c, tmem);
+    mma_role<V41>(P, c, tmem);
   } else if (warp == W_PREP) {
-    prep_role(P, c, lane);
+    prep_role<V41>(P, c, lane);
   }
 
   tc_fence_before();
@@ -1472,7 +1564,10 @@ static int check_params(const dsa_params* p) {
   if (p->topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
   if (!(p->softmax_scale == p->softmax_scale) || !(p->rope_base > 0.f) || !(p->rms_eps >= 0.f))
     return DSA_ERR_INVALID_ARG;
-  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_AFTER_PRODUCER))
+  if (p->kv_format != DSA_KV_FP8_DS_MLA && p->kv_format != DSA_KV_NVFP4_DS_MLA) return DSA_ERR_INVALID_ARG;
+  if (!(p->cmp_scale == p->cmp_scale) || p->cmp_scale == INFINITY || p->cmp_scale == -INFINITY)
+    return DSA_ERR_INVALID_ARG;
+  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_AFTER_PRODUCER | DSA_FLAG_SF_SWIZZLED))
     return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
@@ -1500,8 +1595,10 @@ static int ensure_smem_attr(int dev) {
   if (dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (!g_attr_done[dev]) {
-    if (cudaFuncSetAttribute(dsa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(dsa_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dsa_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+            cudaSuccess)
       return DSA_ERR_CUDA;
     g_attr_done[dev] = true;
   }
@@ -1589,6 +1686,7 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   K.score_scale_log2 = p->softmax_scale * 1.4426950408889634f;
   K.rms_eps = p->rms_eps;
   K.flags = p->flags;
+  K.cmp_scale = p->cmp_scale;
   K.n_splits = ns;
   K.n_halves = nh;
   K.n_items = p->s_q * nh * ns;
@@ -1612,7 +1710,9 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   }
   cfg.attrs = attr;
   cfg.numAttrs = (ns > 1 || ordered) ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, dsa_fwd_kernel, K) != cudaSuccess) return DSA_ERR_CUDA;
+  const bool v41 = p->kv_format == DSA_KV_NVFP4_DS_MLA;
+  if (cudaLaunchKernelEx(&cfg, v41 ? dsa_fwd_kernel<true> : dsa_fwd_kernel<false>, K) != cudaSuccess)
+    return DSA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }
@@ -1688,6 +1788,8 @@ int dsa_params_init(dsa_params* p, int32_t s_q, int32_t h_q, int32_t topk, int32
   p->rope_base = 10000.f;
   p->rms_eps = 1e-6f;
   p->flags = 0;
+  p->kv_format = DSA_KV_FP8_DS_MLA;
+  p->cmp_scale = 1.0f;
   return DSA_OK;
 }
 

@@ -161,6 +161,16 @@ DSA_DEV uint4 ldg_nc(const void* p) {
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
+DSA_DEV uint2 ldg_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+DSA_DEV uint32_t ldg_nc_u8(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
 // L2 prefetch of the 128-byte line holding p (no ordering with other memory accesses)
 DSA_DEV void prefetch_line_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 DSA_DEV void sts128(uint32_t addr, uint4 v) {
@@ -185,6 +195,27 @@ DSA_DEV void codes16_to_f16(uint4 c, uint32_t* o) {
   o[5] = e4m3x2_to_f16x2(c.z >> 16);
   o[6] = e4m3x2_to_f16x2(c.w & 0xFFFF);
   o[7] = e4m3x2_to_f16x2(c.w >> 16);
+}
+// two E2M1 values (first in the low nibble) -> f16x2; every E2M1 value is exact in fp16
+DSA_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+  return h;
+}
+// 16 E2M1 values (eight in each word, first in the lowest nibble) times their common
+// E4M3 scale -> 8 f16x2 words.  Exact: a product of a 2-bit and a 4-bit significand has
+// at most 6 significant bits and lies in [2^-10, 2688].
+DSA_DEV void fp4x16_to_f16(uint32_t lo8, uint32_t hi8, uint32_t scale_code, uint32_t* o) {
+  const uint32_t s2 = e4m3x2_to_f16x2(scale_code | (scale_code << 8));
+  const __half2 s = *reinterpret_cast<const __half2*>(&s2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = e2m1x2_to_f16x2((lo8 >> (8 * i)) & 0xFF), b = e2m1x2_to_f16x2((hi8 >> (8 * i)) & 0xFF);
+    const __half2 pa = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
+    const __half2 pb = __hmul2(*reinterpret_cast<const __half2*>(&b), s);
+    o[i] = *reinterpret_cast<const uint32_t*>(&pa);
+    o[4 + i] = *reinterpret_cast<const uint32_t*>(&pb);
+  }
 }
 // Two fp32 values as fp16 hi + lo pairs: hi = fp16(x) (nearest even), lo = fp16(x - hi).
 // x - hi is exact in fp32, so hi + lo carries x to about 2^-22 relative (exactly when x

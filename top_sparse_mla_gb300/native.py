@@ -34,6 +34,12 @@ DSA_ROW_BYTES = 656
 DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 DSA_KV_FLAG_CHECK_SLOTS = 1
 DSA_FLAG_AFTER_PRODUCER = 4
+DSA_FLAG_SF_SWIZZLED = 8
+DSA_KV_FP8_DS_MLA = 0
+DSA_KV_NVFP4_DS_MLA = 1
+DSA_NVFP4_QK_DIMS = 512
+DSA_NVFP4_SWA_ROW_BYTES = 528
+DSA_NVFP4_CMP_ROW_BYTES = 288
 DSA_STATUS_SLOT_OUT_OF_RANGE = 4
 
 EXPORTED = (
@@ -62,6 +68,8 @@ class DsaParams(ctypes.Structure):
         ("rope_base", ctypes.c_float),
         ("rms_eps", ctypes.c_float),
         ("flags", ctypes.c_uint32),
+        ("kv_format", ctypes.c_int32),
+        ("cmp_scale", ctypes.c_float),
     ]
 
 
@@ -108,6 +116,11 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_kv_insert.restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+def sf_swizzled_bytes(s_q: int, h_q: int) -> int:
+    """Size of out_sf with DSA_FLAG_SF_SWIZZLED (DSA_SF_SWIZZLED_BYTES in the header)."""
+    return ((int(s_q) + 127) // 128) * 128 * 16 * int(h_q)
 
 
 def dsa_error_string(code: int) -> str:
