@@ -412,7 +412,7 @@ def run_native(args):
 
     per_config = {}
     if not args.skip_sweep and world == 1:
-        for name in ("decode1", "decode64", "decode1024", "prefill2123", "decode1024_nvfp4"):
+        for name in ("decode1", "decode64", "decode1024", "prefill2123", "decode1024_nvfp4", "decode1024_fp8q"):
             wc = W.make(name) if name != args.workload else w
             ic = api.upload(wc, "cuda") if name != args.workload else inp
             oc = api.allocate_outputs(ic)

@@ -110,6 +110,17 @@ extern "C" {
  * m >= s_q (the last tile row's padding) are not written.  The codes themselves, and
  * every other output, are those of the row-major layout. */
 #define DSA_FLAG_SF_SWIZZLED 8u
+/* Quantise q's latent part to E4M3 inside the kernel before QK^T, the "query FP8
+ * quantization inside the sparse-MLA kernel" of "DSV4.1 latency_specialized decode at
+ * TP4 on GB300" (vLLM PR #64364, "The changes and what each bought", Attention row);
+ * the rule is this library's reading.  Per token and head, over the 512 latent dims:
+ * amax = max |q * norm_w| and code = E4M3(fl(q * norm_w) * fl(448 / amax)), round to
+ * nearest even, saturating, every step in binary32 (q * norm_w is exact).  This is the
+ * RMSNorm'd latent divided by its scale s = amax * rms_inv / 448 (the RMS factor
+ * cancels), and the latent part of q~ is then code * s.  The rope dims stay as without
+ * the flag (the keys' rope part is bf16).  Everything else is unchanged, so the result is
+ * step 5 on that q~.  Only with DSA_KV_FP8_DS_MLA (DSA_ERR_INVALID_ARG otherwise). */
+#define DSA_FLAG_FP8_Q 16u
 #define DSA_SF_SWIZZLED_BYTES(s_q, h_q) ((((size_t)(s_q) + 127) / 128) * 128 * 16 * (size_t)(h_q))
 
 #define DSA_STATUS_INDEX_OUT_OF_RANGE 1u /* an index was >= its pool size (with the flag) */

@@ -49,6 +49,7 @@ class OracleParams:
     softmax_scale: float = 1.0 / np.sqrt(D_QK)
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
+    fp8_q: bool = False       # E4M3 latent q (quantize_q_latent)
 
 
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
@@ -84,14 +85,40 @@ def rope_interleaved(x: np.ndarray, pos: float, base: float, inverse: bool = Fal
     return y
 
 
+def quantize_q_latent(q_bits: np.ndarray, norm_w_bits: np.ndarray):
+    """E4M3 codes of q's latent part, per head: (codes uint8 [h, 512], amax float32 [h]).
+
+    The query FP8 quantisation named on "DSV4.1 latency_specialized decode at TP4 on
+    GB300" (vLLM PR #64364, "The changes and what each bought", Attention row); the page
+    gives no rule, the reading taken: per token and head, amax = max |q * w| over the 512
+    latent dims and code = E4M3(fl(q * w) * fl(448 / amax)), ties to even, saturating,
+    each step in binary32.  The RMSNorm'd latent is then code * amax * rms_inv / 448
+    (the RMS factor cancels in the code).  An all-zero latent gives codes 0.
+    """
+    x = codecs.bf16_decode(q_bits[..., :D_LATENT]).astype(np.float32)
+    w = codecs.bf16_decode(norm_w_bits[:D_LATENT]).astype(np.float32)
+    xw = x * w                                          # exact in binary32
+    amax = np.max(np.abs(xw), axis=-1)
+    safe = np.where(amax > 0, amax, np.float32(1.0))
+    rq = np.where(amax > 0, np.float32(448.0) / safe, np.float32(0.0)).astype(np.float32)
+    y = (xw * rq[..., None]).astype(np.float32)
+    return codecs.e4m3_encode(y.astype(np.float64)), amax
+
+
 def q_prologue(q_bits: np.ndarray, norm_w_bits: np.ndarray, pos: int, p: OracleParams) -> np.ndarray:
-    """Steps 1-2 for one token: bf16 q [h, 576] -> normalised, rotated q~ [h, 576].
+    """Steps 1-2 for one token: bf16 q [h, 576] -> normalised, rotated q~ [h, 576].  With
+    p.fp8_q the latent dims are replaced by their E4M3 values (quantize_q_latent) times
+    the head's scale amax * rms_inv / 448.
 
     Steps 1-2 of "Deepseek V41 Attention MegaKernel" (vLLM PR #56344), Purpose.
     """
     x = codecs.bf16_decode(q_bits)
     w = codecs.bf16_decode(norm_w_bits)
     xn = rmsnorm(x, w, p.rms_eps)
+    if p.fp8_q:
+        codes, amax = quantize_q_latent(q_bits, norm_w_bits)
+        rms_inv = 1.0 / np.sqrt(np.mean(x * x, axis=-1) + p.rms_eps)
+        xn[..., :D_LATENT] = codecs.e4m3_decode(codes) * (amax.astype(np.float64) * rms_inv / 448.0)[..., None]
     xn[..., D_LATENT:] = rope_interleaved(xn[..., D_LATENT:], pos, p.rope_base)
     return xn
 

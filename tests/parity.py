@@ -55,7 +55,7 @@ def subset(w: Workload, tokens) -> Workload:
     return Workload(name=w.name + "_subset", q=w.q[tokens], norm_w=w.norm_w, kv_swa=w.kv_swa, kv_cmp=w.kv_cmp,
                     indices=w.indices[tokens], topk_length=w.topk_length[tokens], positions=w.positions[tokens],
                     n_swa_cols=w.n_swa_cols, seed=w.seed, kv_format=w.kv_format, cmp_scale=w.cmp_scale,
-                    softmax_scale=w.softmax_scale)
+                    softmax_scale=w.softmax_scale, fp8_q=w.fp8_q)
 
 
 def run_oracle(w: Workload):
@@ -64,7 +64,7 @@ def run_oracle(w: Workload):
         return oracle.nvfp4.sparse_mla_forward(w.q, w.kv_swa, w.kv_cmp, w.indices, w.topk_length, w.positions,
                                                w.norm_w, p, cmp_scale=w.cmp_scale)
     return oracle.sparse_mla_forward(w.q, w.kv_swa, w.kv_cmp, w.indices, w.topk_length, w.positions, w.norm_w,
-                                     oracle.OracleParams(n_swa_cols=w.n_swa_cols))
+                                     oracle.OracleParams(n_swa_cols=w.n_swa_cols, fp8_q=w.fp8_q))
 
 
 def near_power_of_two(amax: np.ndarray, rel: float = SF_BAND_REL) -> np.ndarray:

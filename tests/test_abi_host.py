@@ -59,9 +59,9 @@ def test_flag_mask(lib):
     # the defined flags pass the argument check (num_splits returns 0 on a bad argument)
     p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096,
                                flags=native.DSA_FLAG_CHECK_INDICES | native.DSA_FLAG_TEST_WAIT_TIMEOUT
-                               | native.DSA_FLAG_AFTER_PRODUCER | native.DSA_FLAG_SF_SWIZZLED)
+                               | native.DSA_FLAG_AFTER_PRODUCER | native.DSA_FLAG_SF_SWIZZLED | native.DSA_FLAG_FP8_Q)
     assert native.dsa_sparse_attn_num_splits(p, 152) == 8
-    for bad in (16, 32, 1 << 31):
+    for bad in (32, 64, 1 << 31):
         p.flags = bad
         assert native.dsa_sparse_attn_num_splits(p, 152) == 0
 
@@ -190,7 +190,7 @@ def test_argument_validation_happens_before_any_gpu_work(lib):
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
     p = native.dsa_params_init(2, 64, 640, 128, 1 << 31, 2000)
     assert _call(lib, p) == native.DSA_ERR_UNSUPPORTED_SHAPE
-    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, flags=16)
+    p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, flags=32)
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
     p = native.dsa_params_init(2, 64, 640, 128, 1000, 2000, softmax_scale=float("nan"))
     assert _call(lib, p) == native.DSA_ERR_INVALID_ARG
@@ -218,3 +218,10 @@ def test_cache_format_arguments(lib):
         assert native.dsa_sparse_attn_num_splits(p, 152) == 0
     p.cmp_scale = 0.0
     assert native.dsa_sparse_attn_num_splits(p, 152) == 8
+
+
+def test_fp8_q_needs_the_fp8_ds_mla_cache(lib):
+    p = native.dsa_params_init(4, 64, 1024, 128, 512, 4096, flags=native.DSA_FLAG_FP8_Q)
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 8
+    p.kv_format = native.DSA_KV_NVFP4_DS_MLA
+    assert native.dsa_sparse_attn_num_splits(p, 152) == 0

@@ -46,7 +46,7 @@ def _dev(a: np.ndarray, device, dtype):
 def upload(w: Workload, device="cuda", flags: int = 0) -> DeviceInputs:
     # uint16 bit patterns travel as int16 (torch has no general uint16 ops)
     p = native.dsa_params_init(w.s_q, w.h_q, w.topk, w.n_swa_cols, w.kv_swa.shape[0], w.kv_cmp.shape[0])
-    p.flags = flags
+    p.flags = flags | (native.DSA_FLAG_FP8_Q if w.fp8_q else 0)
     p.kv_format = w.kv_format
     p.cmp_scale = w.cmp_scale
     p.softmax_scale = w.softmax_scale

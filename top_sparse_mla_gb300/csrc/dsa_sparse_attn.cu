@@ -89,7 +89,8 @@ constexpr uint32_t SM_V = SM_Q + 9 * 8192;         // codes tile: 4 chunks x 2 h
 constexpr uint32_t SM_P = SM_V + 4 * 32768;        // P_0 / P_2: [128 rows x 64] fp16
 constexpr uint32_t SM_ROPE = SM_P + 16384;         // NB x 32 x (cos, sin)
 constexpr uint32_t SM_INV = SM_ROPE + NB * 256;    // NB x 32 fp32 score factors
-constexpr uint32_t SM_ITEM = SM_INV + NB * 128;    // NB x 16 ints
+constexpr uint32_t SM_RATIO = SM_INV + NB * 128;   // NB x 32 fp32 latent-to-rope score ratios (FP8 q)
+constexpr uint32_t SM_ITEM = SM_RATIO + NB * 128;  // NB x 16 ints
 constexpr uint32_t SM_M = SM_ITEM + NB * 64;       // 32 fp32 running max (log2 units)
 constexpr uint32_t SM_ALPHA = SM_M + 128;          // 32 fp32 rescale factors
 constexpr uint32_t SM_RED = SM_ALPHA + 128;        // 2 groups x 4 warps x 16 fp32
@@ -605,7 +606,13 @@ struct QArgs {
   float eps, c2;
 };
 
-template <bool V41>
+// With FP8Q (DSA_FLAG_FP8_Q) the latent rows of q~ hold E4M3 values instead (hi only, no
+// lo part): code = E4M3(fl(q * w) * fl(448 / amax)), amax = the head's largest |q * w| over
+// the 512 latent dims, decided in binary32 (the RMS factor cancels: this is the head's
+// RMSNorm'd latent divided by its scale amax * rms / 448).  The rope part stays as above,
+// and SM_RATIO[b][head] = 2^k / fl(448 / amax) turns the latent scores into the rope
+// part's units.
+template <bool V41, bool FP8Q>
 DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
   constexpr int d_q = Fmt<V41>::d_q;         // 576 (rotary atom 8) or 512 (rotary atom 7)
   const int* info = item_info(c, b);
@@ -620,8 +627,8 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
   uint4 raw[9];
 #pragma unroll
   for (int a = 0; a < 9; ++a) raw[a] = (hv && a < na) ? ldg_nc(qh + 64 * a) : make_uint4(0, 0, 0, 0);
-  // pass 1: sum of squares of q, largest |q * w|
-  float ss = 0.f, amax = 0.f;
+  // pass 1: sum of squares of q, largest |q * w| (and over the latent dims alone)
+  float ss = 0.f, amax = 0.f, amax_lat = 0.f;
 #pragma unroll
   for (int a = 0; a < 9; ++a) {
     const uint4 wq = a < na ? ldg_nc(wp + 64 * a) : make_uint4(0, 0, 0, 0);
@@ -631,8 +638,9 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
     for (int e = 0; e < 4; ++e) {
       const float x0 = __uint_as_float(x4[e] << 16), x1 = __uint_as_float(x4[e] & 0xFFFF0000u);
       ss = fmaf(x0, x0, fmaf(x1, x1, ss));
-      amax = fmaxf(amax, fmaxf(fabsf(x0 * __uint_as_float(w4[e] << 16)),
-                               fabsf(x1 * __uint_as_float(w4[e] & 0xFFFF0000u))));
+      const float m = fmaxf(fabsf(x0 * __uint_as_float(w4[e] << 16)), fabsf(x1 * __uint_as_float(w4[e] & 0xFFFF0000u)));
+      amax = fmaxf(amax, m);
+      if (FP8Q && a < 8) amax_lat = fmaxf(amax_lat, m);
     }
   }
   ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
@@ -641,6 +649,13 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  float rq = 0.f;   // fl(448 / amax_lat): the latent's quantisation factor (FP8Q)
+  if constexpr (FP8Q) {
+    amax_lat = fmaxf(amax_lat, __shfl_xor_sync(0xFFFFFFFFu, amax_lat, 1));
+    amax_lat = fmaxf(amax_lat, __shfl_xor_sync(0xFFFFFFFFu, amax_lat, 2));
+    amax_lat = fmaxf(amax_lat, __shfl_xor_sync(0xFFFFFFFFu, amax_lat, 4));
+    rq = amax_lat > 0.f ? __fdiv_rn(448.0f, amax_lat) : 0.f;
+  }
   const int ea = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // floor(log2 amax) + 127 (normal amax)
   int k = ea == 0 ? 0 : 140 - ea;
   k = k < -100 ? -100 : (k > 100 ? 100 : k);
@@ -657,6 +672,23 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
     const uint4 wq = ldg_nc(wp + 64 * a);
     const uint32_t x4[4] = {raw[a].x, raw[a].y, raw[a].z, raw[a].w};
     const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+    if (FP8Q && a < 8) {
+      // E4M3 codes of the latent dims, as exact fp16 values in the hi rows only
+      uint32_t hw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y0 = __fmul_rn(__uint_as_float(x4[e] << 16) * __uint_as_float(w4[e] << 16), rq);
+        const float y1 = __fmul_rn(__uint_as_float(x4[e] & 0xFFFF0000u) * __uint_as_float(w4[e] & 0xFFFF0000u), rq);
+        hw[e] = e4m3x2_to_f16x2(f32x2_to_e4m3x2(y0, y1));
+      }
+      const uint32_t atom = c.sb + SM_Q + (uint32_t)a * 8192 + ((uint32_t)chn ^ (uint32_t)(hs & 7)) * 16u;
+      sts128(atom + (uint32_t)(hs >> 3) * 1024 + (uint32_t)(hs & 7) * 128, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      if ((a & 1) == 1) {
+        fence_async_smem();
+        arrive_w(c, B_QRDY + (a >> 1));
+      }
+      continue;
+    }
     float x[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -687,6 +719,7 @@ DSA_DEV void build_q(const QArgs& P, const Ctx& c, int b, int er) {
   float* s_inv = reinterpret_cast<float*>(c.sm + SM_INV) + 32 * b;
   if (chn == 0) s_inv[hs] = hv ? rsqrtf(ss * (1.0f / d_q) + P.eps) * P.c2 * __uint_as_float((uint32_t)(127 - k) << 23)
                                : 0.f;
+  if (FP8Q && chn == 0) reinterpret_cast<float*>(c.sm + SM_RATIO)[32 * b + hs] = rq > 0.f ? __fdiv_rn(sk, rq) : 0.f;
   arrive_w(c, B_QSTAT + b);
 }
 
@@ -732,7 +765,7 @@ DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const Dq
   }
 }
 
-template <bool V41>
+template <bool V41, bool FP8Q>
 DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int lane) {
   const int sub = lane >> 3, ch = lane & 7;
   const uint32_t half_off = (uint32_t)(ch >> 2) * 16384;
@@ -775,7 +808,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       if (info[IT_ITEM] < 0) return 0;
       if (info[IT_T] > 0) {
         if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
-        build_q<V41>(qa, c, b, 32 * w + lane);
+        build_q<V41, FP8Q>(qa, c, b, 32 * w + lane);
         dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, cur);
         dq_load_chunk<V41>(P, raw[0], qk_chunk(0), cur, ch);
         dq_load_chunk<V41>(P, raw[1], qk_chunk(1), cur, ch);
@@ -896,9 +929,11 @@ DSA_DEV void commit(uint32_t bar_addr) {
   __syncwarp();
 }
 
-template <bool V41>
+template <bool V41, bool FP8Q>
 DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
   constexpr uint32_t IDESC_QK = idesc_f16(128, NQ, 0, 0);
+  // the latent partials: N = 32 with an E4M3 q (its rows hold no lo part)
+  constexpr uint32_t IDESC_QK_LAT = FP8Q ? idesc_f16(128, NQ / 2, 0, 0) : IDESC_QK;
   constexpr uint32_t IDESC_PV = idesc_f16(128, NQ, 1, 1);
   // every descriptor of the loop is one of these plus a constant offset (in 16-byte units
   // in the low 14-bit address field; no offset used here carries out of it)
@@ -931,7 +966,7 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = cidx * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
           const uint32_t boff = (2 * cidx + (kk >> 2)) * 8192 + (kk & 3) * 32;
-          issue_ss(d_s, d_k + (aoff >> 4), d_q + (boff >> 4), IDESC_QK, kk ? 1u : 0u);
+          issue_ss(d_s, d_k + (aoff >> 4), d_q + (boff >> 4), IDESC_QK_LAT, kk ? 1u : 0u);
         }
         commit(bar(c, B_SFULL + sbf));
         ++np;
@@ -1037,7 +1072,7 @@ DSA_DEV void store_pb(uint32_t base, int r, int gq, const float (&p)[16], float 
   }
 }
 
-template <bool V41>
+template <bool V41, bool FP8Q>
 DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int q4, int lane) {
   const int r = q4 * 32 + lane;
   const int hb = 16 * gq;                       // the group's first head within the item
@@ -1118,6 +1153,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
     // (one phase of QSTAT[b] per use of item buffer b: the next needs this buffer released)
     if (!wait_bar_w(c, B_QSTAT + b, (seq / NB) & 1)) return;
     const float* s_inv = reinterpret_cast<const float*>(c.sm + SM_INV) + 32 * b + hb;
+    const float* s_ratio = reinterpret_cast<const float*>(c.sm + SM_RATIO) + 32 * b + hb;
     if (r < 16) s_m[hb + r] = -INFINITY;
     float lw = 0.f;   // this warp's row sum of head hb + lane / 2
     if (!grp.sync(c)) return;
@@ -1140,12 +1176,21 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         const uint32_t ts = tmem + tlane + TM_S + 64 * sbf + hb;
         uint32_t a[16], l[16];
         tmem_ld16(ts, a);
-        tmem_ld16(ts + HH, l);
+        if (!FP8Q || p == 4) tmem_ld16(ts + HH, l);   // (an E4M3 q's latent partials have no lo part)
         tc_wait_ld();
         tc_fence_before();
         arrive_w(c, B_SFREE + sbf);
+        if (FP8Q && p < 4) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[i]);
+          for (int i = 0; i < 16; ++i) y[i] = fmaf(f, __uint_as_float(a[i]), y[i]);
+        } else if (FP8Q) {
+          // the rope partial; the latent sum into the rope part's units first
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = fmaf(y[i], s_ratio[i], __uint_as_float(a[i]) + __uint_as_float(l[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = fmaf(f, __uint_as_float(a[i]) + __uint_as_float(l[i]), y[i]);
+        }
         ++np;
       }
       // scores in log2 units (without the running max)
@@ -1402,7 +1447,7 @@ __global__ void __launch_bounds__(ORDER_THREADS, 1) dsa_order_kernel(const int32
   }
 }
 
-template <bool V41>
+template <bool V41, bool FP8Q>
 __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
@@ -1460,11 +1505,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < W_SX) {
-    dq_role<V41>(P, c, tmem, warp, lane);
+    dq_role<V41, FP8Q>(P, c, tmem, warp, lane);
   } else if (warp < W_MMA) {
-    sx_role<V41>(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
+    sx_role<V41, FP8Q>(P, c, tmem, (warp - W_SX) >> 2, warp & 3, lane);
   } else if (warp == W_MMA) {
-    mma_role<V41>(P, c, tmem);
+    mma_role<V41, FP8Q>(P, c, tmem);
   } else if (warp == W_PREP) {
     prep_role<V41>(P, c, lane);
   }
@@ -1565,9 +1610,11 @@ static int check_params(const dsa_params* p) {
   if (!(p->softmax_scale == p->softmax_scale) || !(p->rope_base > 0.f) || !(p->rms_eps >= 0.f))
     return DSA_ERR_INVALID_ARG;
   if (p->kv_format != DSA_KV_FP8_DS_MLA && p->kv_format != DSA_KV_NVFP4_DS_MLA) return DSA_ERR_INVALID_ARG;
+  if ((p->flags & DSA_FLAG_FP8_Q) && p->kv_format != DSA_KV_FP8_DS_MLA) return DSA_ERR_INVALID_ARG;
   if (!(p->cmp_scale == p->cmp_scale) || p->cmp_scale == INFINITY || p->cmp_scale == -INFINITY)
     return DSA_ERR_INVALID_ARG;
-  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_AFTER_PRODUCER | DSA_FLAG_SF_SWIZZLED))
+  if (p->flags & ~(DSA_FLAG_CHECK_INDICES | DSA_FLAG_TEST_WAIT_TIMEOUT | DSA_FLAG_AFTER_PRODUCER | DSA_FLAG_SF_SWIZZLED |
+                   DSA_FLAG_FP8_Q))
     return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
@@ -1595,10 +1642,12 @@ static int ensure_smem_attr(int dev) {
   if (dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (!g_attr_done[dev]) {
-    if (cudaFuncSetAttribute(dsa_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(dsa_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(dsa_fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa_fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa_fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
       return DSA_ERR_CUDA;
     g_attr_done[dev] = true;
   }
@@ -1710,9 +1759,11 @@ static int launch(const void* q, const void* kv_swa, const void* kv_cmp, const i
   }
   cfg.attrs = attr;
   cfg.numAttrs = (ns > 1 || ordered) ? 1 : 0;
-  const bool v41 = p->kv_format == DSA_KV_NVFP4_DS_MLA;
-  if (cudaLaunchKernelEx(&cfg, v41 ? dsa_fwd_kernel<true> : dsa_fwd_kernel<false>, K) != cudaSuccess)
-    return DSA_ERR_CUDA;
+  // one instantiation per cache format, and the fp8_ds_mla one also with an E4M3 q
+  void (*kernel)(KParams) = p->kv_format == DSA_KV_NVFP4_DS_MLA ? dsa_fwd_kernel<true, false>
+                            : (p->flags & DSA_FLAG_FP8_Q)       ? dsa_fwd_kernel<false, true>
+                                                                : dsa_fwd_kernel<false, false>;
+  if (cudaLaunchKernelEx(&cfg, kernel, K) != cudaSuccess) return DSA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }

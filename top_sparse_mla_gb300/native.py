@@ -35,6 +35,7 @@ DSA_NOALLOC_SCRATCH_BYTES = 24 << 20
 DSA_KV_FLAG_CHECK_SLOTS = 1
 DSA_FLAG_AFTER_PRODUCER = 4
 DSA_FLAG_SF_SWIZZLED = 8
+DSA_FLAG_FP8_Q = 16
 DSA_KV_FP8_DS_MLA = 0
 DSA_KV_NVFP4_DS_MLA = 1
 DSA_NVFP4_QK_DIMS = 512

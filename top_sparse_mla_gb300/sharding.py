@@ -29,4 +29,4 @@ def shard(w: Workload, rank: int, world: int) -> Workload:
     return Workload(name=f"{w.name}_r{rank}of{world}", q=w.q[sel], norm_w=w.norm_w, kv_swa=w.kv_swa,
                     kv_cmp=w.kv_cmp, indices=w.indices[sel], topk_length=w.topk_length[sel],
                     positions=w.positions[sel], n_swa_cols=w.n_swa_cols, seed=w.seed, kv_format=w.kv_format,
-                    cmp_scale=w.cmp_scale, softmax_scale=w.softmax_scale)
+                    cmp_scale=w.cmp_scale, softmax_scale=w.softmax_scale, fp8_q=w.fp8_q)

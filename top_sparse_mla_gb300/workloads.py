@@ -63,6 +63,7 @@ class Workload:
     kv_format: int = 0              # 0: fp8_ds_mla (656-byte rows), 1: nvfp4_ds_mla (528 / 288)
     cmp_scale: float = 1.0          # nvfp4_ds_mla: fp32 scale of every kv_cmp value
     softmax_scale: float = 1.0 / 24.0   # 1/sqrt(576); 1/sqrt(512) for nvfp4_ds_mla
+    fp8_q: bool = False             # q's latent quantised to E4M3 in the kernel (DSA_FLAG_FP8_Q)
 
     @property
     def s_q(self) -> int:
@@ -312,8 +313,22 @@ CONFIGS = {
     "decode1024": config_decode1024,
     "prefill2123": config_prefill2123,
 }
-# the same shapes, index patterns and seeds on the nvfp4_ds_mla (V4.1) cache
-CONFIGS.update({k + "_nvfp4": (lambda f: (lambda: f(kv_format=1)))(f) for k, f in list(CONFIGS.items())})
+# the same shapes, index patterns and seeds on the nvfp4_ds_mla (V4.1) cache, and with
+# an E4M3 q (the same inputs; only the kernel's flag and the oracle's reading differ)
+_BASE = dict(CONFIGS)
+CONFIGS.update({k + "_nvfp4": (lambda f: (lambda: f(kv_format=1)))(f) for k, f in _BASE.items()})
+
+
+def _with_fp8_q(f):
+    def make_it():
+        w = f()
+        w.fp8_q = True
+        w.name += "_fp8q"
+        return w
+    return make_it
+
+
+CONFIGS.update({k + "_fp8q": _with_fp8_q(f) for k, f in _BASE.items()})
 
 
 def make(name: str) -> Workload:
