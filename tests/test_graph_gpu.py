@@ -23,11 +23,11 @@ def _direct(inp):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "decode1"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "tiny_nvfp4", "decode1_nvfp4", "tiny_fp8q"])
 def test_forward_replays_from_a_cuda_graph(name):
     w = W.make(name)
     inp = api.upload(w, "cuda:0")
-    if name == "decode1":
+    if name.startswith("decode1"):
         p = native.dsa_params_init(w.s_q, w.h_q, w.topk, w.n_swa_cols, w.kv_swa.shape[0], w.kv_cmp.shape[0])
         assert native.dsa_sparse_attn_num_splits(p) > 1
     ref_fp8, ref_sf = _direct(inp)

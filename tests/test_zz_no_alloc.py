@@ -77,6 +77,13 @@ def test_unsplit_path_two_calls_in_a_row():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("name", ["decode1_nvfp4", "decode64_nvfp4", "decode1_fp8q", "decode64_fp8q"])
+def test_other_kernel_instantiations_two_calls_in_a_row(name):
+    # the nvfp4_ds_mla cache and the E4M3-q option (the kernel's other two instantiations)
+    assert _check_case(W.make(name)) == 0
+
+
+@pytest.mark.gpu
 def test_status_word_reaches_status_out():
     w = W.random_case(405, s_q=2, h_q=16, n_swa_cols=16, n_cmp_cols=48, n_swa_rows=64, n_cmp_rows=128)
     w.indices[1, 20] = w.kv_cmp.shape[0] + 7       # out of range for its pool
