@@ -54,11 +54,14 @@ def _timed_out_run(w):
     return g
 
 
-def test_wait_timeout_without_splits_reports_and_recovers():
+@pytest.mark.parametrize("variant", ["fp8_ds_mla", "nvfp4_ds_mla", "fp8_q"])
+def test_wait_timeout_without_splits_reports_and_recovers(variant):
     # 128 index columns: one tile, so no token is split; CTA 0 takes no item and the
-    # other seven CTAs compute all eight tokens
+    # other seven CTAs compute all eight tokens (on each of the kernel's instantiations)
     w = W.random_case(411, s_q=8, h_q=64, n_swa_cols=32, n_cmp_cols=96, n_swa_rows=256, n_cmp_rows=512,
-                      n_sentinels=5)
+                      n_sentinels=5, kv_format=1 if variant == "nvfp4_ds_mla" else 0,
+                      cmp_scale=0.75 if variant == "nvfp4_ds_mla" else 1.0)
+    w.fp8_q = variant == "fp8_q"
     assert _splits(w) == 1
     clean = parity.run_gpu(w)
     assert clean["status"] == 0

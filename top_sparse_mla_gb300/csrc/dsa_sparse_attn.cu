@@ -308,6 +308,17 @@ __device__ __noinline__ void write_empty_item(const KParams& P, int t, int half,
   if (P.out_lse && lane < nh) P.out_lse[(size_t)t * P.h_q + h0 + lane] = -INFINITY;
 }
 
+// (cos, sin) of positions[t] * theta_i, from an exact fixed-point count of turns
+// (rope_turns[i]: the fraction of theta_i / 2 pi in units of 2^-64; the top 24 bits of the
+// product are the fraction of a turn).
+DSA_DEV float2 rope_entry_of(const KParams& P, int t, int i) {
+  const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[i];
+  const float frac = (float)(turns >> 40) * 5.9604644775390625e-08f;   // top 24 bits / 2^24
+  float sn, cs;
+  sincospif(2.0f * frac, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
 DSA_DEV uint32_t redux_max_u32(uint32_t v) {
   uint32_t r;
   asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
@@ -432,15 +443,7 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
       e = e < 1 ? 1 : (e > 253 ? 253 : e);
       ebits[k] = (uint32_t)e;
     }
-    // cos / sin of positions[t] * theta_i from an exact fixed-point count of turns
-    {
-      float2* rope = reinterpret_cast<float2*>(c.sm + SM_ROPE) + 32 * b;
-      const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[lane];
-      const float frac = (float)(turns >> 40) * 5.9604644775390625e-08f;   // top 24 bits / 2^24
-      float sn, cs;
-      sincospif(2.0f * frac, &sn, &cs);
-      rope[lane] = make_float2(cs, sn);
-    }
+    reinterpret_cast<float2*>(c.sm + SM_ROPE)[32 * b + lane] = rope_entry_of(P, t, lane);
     if (lane == 0) {
       info[IT_ITEM] = item;
       info[IT_TOKEN] = t;
@@ -458,12 +461,14 @@ DSA_DEV void prep_role(const KParams& P, const Ctx& c, int lane) {
   }
 }
 
-// Finish 32 consecutive output dims of one head in one thread: inverse RoPE, optional
-// pre-cast store, MXFP8 (one 32-value block) and the stores.
-DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int d0, const float2* rope) {
+// Finish eight consecutive output dims d0 .. d0 + 7 of head h in one of the four lanes
+// (gmask) that share a 32-dim MXFP8 block: inverse RoPE, optional pre-cast store, the
+// block amax across the four lanes, the UE8M0 code (stored by the block's first lane) and
+// eight E4M3 codes.
+DSA_DEV void finalize_eighth(const OutPtrs& O, float (&v)[8], int t, int h, int d0, unsigned gmask, const float2* rope) {
   if (d0 >= 448) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < 4; ++k) {
       const float2 cs = rope[((d0 - 448) >> 1) + k];
       const float x0 = v[2 * k], x1 = v[2 * k + 1];
       v[2 * k] = fmaf(x1, cs.y, x0 * cs.x) + 0.0f;     // +0.0f: a rotated exact zero stays +0
@@ -473,26 +478,26 @@ DSA_DEV void finalize_block(const OutPtrs& O, float (&v)[32], int t, int h, int 
   const size_t row = (size_t)t * O.h_q + h;
   if (O.precast) {
     float4* dst = reinterpret_cast<float4*>(O.precast + row * D_LAT + d0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
   float amax = 0.f;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
   int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 8;   // floor(log2 amax) - 8
   E = E < -127 ? -127 : E;
   const float inv = __uint_as_float((uint32_t)(127 - E) << 23);    // 2^-E, exact
-  uint32_t wq[8];
+  uint32_t wq[2];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < 2; ++k) {
     const uint32_t lo = f32x2_to_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv);
     const uint32_t hi = f32x2_to_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv);
     wq[k] = lo | (hi << 16);
   }
-  uint4* dst = reinterpret_cast<uint4*>(O.fp8 + row * D_LAT + d0);
-  dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-  dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-  O.sf[sf_offset(O, t, h, d0 >> 5)] = (uint8_t)(E + 127);
+  *reinterpret_cast<uint2*>(O.fp8 + row * D_LAT + d0) = make_uint2(wq[0], wq[1]);
+  if ((d0 & 31) == 0) O.sf[sf_offset(O, t, h, d0 >> 5)] = (uint8_t)(E + 127);
 }
 
 // Finish dim d of heads h0..h0+N-1, one head per register; the 32 lanes of the warp hold
@@ -1312,69 +1317,74 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
 }
 
 // Combine of one (token, half)'s split partials: split `part` takes the slice
-// part / n_splits of its (head, 32-dim block) units, one unit per thread; weights
-// exp2(lse_s - M) / sum over splits.
+// part / n_splits of its (head, 32-dim block) units, four threads per unit (eight dims
+// each); weights exp2(lse_s - M) / sum over splits.  The token's rotary table is already
+// in s_rope (written while the splits were still arriving).
 DSA_DEV void combine_token(const KParams& P, const Ctx& c, int t, int half, int part, int tid) {
   float* s_cw = reinterpret_cast<float*>(c.sm + SM_CW);       // [MAX_SPLITS][32]
   float* s_lse = s_cw + MAX_SPLITS * HH;                       // [32]
-  float2* s_rope = reinterpret_cast<float2*>(s_lse + HH);      // [32] (cos, sin)
+  const float2* s_rope = reinterpret_cast<const float2*>(s_lse + HH);   // [32] (cos, sin)
   const int ns = P.n_splits;
   const int h0 = HH * half;
   const float ln2 = 0.69314718055994531f;
   if (tid < HH) {
     const float* pl = P.part_lse + (size_t)t * ns * 64 + h0 + tid;
+    float lv[MAX_SPLITS];
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) lv[s] = s < ns ? __ldcg(pl + s * 64) : -INFINITY;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(pl + s * 64));
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) M = fmaxf(M, lv[s]);
     float den = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = (M == -INFINITY) ? 0.f : exp2f(__ldcg(pl + s * 64) - M);
-      s_cw[s * HH + tid] = w;
-      den += w;
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) {
+      lv[s] = (M == -INFINITY || s >= ns) ? 0.f : exp2f(lv[s] - M);
+      den += lv[s];
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int s = 0; s < ns; ++s) s_cw[s * HH + tid] *= inv;
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s)
+      if (s < ns) s_cw[s * HH + tid] = lv[s] * inv;
     s_lse[tid] = den > 0.f ? (M + log2f(den)) * ln2 : -INFINITY;
   }
   __syncthreads();
   if (part == 0 && P.out_lse && tid < HH && h0 + tid < P.h_q) P.out_lse[(size_t)t * P.h_q + h0 + tid] = s_lse[tid];
-  // the rotary table of this token, rebuilt (the item buffers are gone)
-  if (tid < 32) {
-    const unsigned long long turns = (unsigned long long)(long long)P.positions[t] * P.rope_turns[tid];
-    const float frac = (float)(turns >> 40) * 5.9604644775390625e-08f;
-    float sn, cs;
-    sincospif(2.0f * frac, &sn, &cs);
-    s_rope[tid] = make_float2(cs, sn);
-  }
-  __syncthreads();
-  const float2* rope = s_rope;
   const int nh = (P.h_q - h0) < HH ? (P.h_q - h0) : HH;
   const int u0 = part * nh * 16 / ns, u1 = (part + 1) * nh * 16 / ns;
-  for (int u = u0 + tid; u < u1; u += NTHREADS) {
+  const int q = tid & 3;                                         // this thread's eight dims of the unit
+  const unsigned gmask = 0xFu << (tid & 28);                     // the unit's four lanes
+  for (int u = u0 + (tid >> 2); u < u1; u += NTHREADS / 4) {
     const int hh = u >> 4, blk = u & 15;
-    float v[32];
+    float v[8];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = 0.f;
-    const float* base = P.part_o + ((size_t)t * ns * 64 + h0 + hh) * D_LAT + 32 * blk;
+    for (int k = 0; k < 8; ++k) v[k] = 0.f;
+    const float* base = P.part_o + ((size_t)t * ns * 64 + h0 + hh) * D_LAT + 32 * blk + 8 * q;
+    // four splits' loads in flight at a time
 #pragma unroll 1
-    for (int s = 0; s < ns; s += 2) {
-      const float w0 = s_cw[s * HH + hh];
-      const float w1 = (s + 1 < ns) ? s_cw[(s + 1) * HH + hh] : 0.f;
-      float4 f0[8], f1[8];
-      const float4* src0 = reinterpret_cast<const float4*>(base + (size_t)s * 64 * D_LAT);
-      const float4* src1 = reinterpret_cast<const float4*>(base + (size_t)(s + 1) * 64 * D_LAT);
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+      float w[4];
+      float4 f[4][2];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f0[k] = w0 != 0.f ? __ldcg(src0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 4; ++j) {
+        const int sp = s0 + j;
+        w[j] = sp < ns ? s_cw[sp * HH + hh] : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(base + (size_t)sp * 64 * D_LAT);
+        f[j][0] = w[j] != 0.f ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[j][1] = w[j] != 0.f ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f1[k] = w1 != 0.f ? __ldcg(src1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        v[4 * k] = fmaf(w0, f0[k].x, fmaf(w1, f1[k].x, v[4 * k]));
-        v[4 * k + 1] = fmaf(w0, f0[k].y, fmaf(w1, f1[k].y, v[4 * k + 1]));
-        v[4 * k + 2] = fmaf(w0, f0[k].z, fmaf(w1, f1[k].z, v[4 * k + 2]));
-        v[4 * k + 3] = fmaf(w0, f0[k].w, fmaf(w1, f1[k].w, v[4 * k + 3]));
+      for (int j = 0; j < 4; ++j) {
+        v[0] = fmaf(w[j], f[j][0].x, v[0]);
+        v[1] = fmaf(w[j], f[j][0].y, v[1]);
+        v[2] = fmaf(w[j], f[j][0].z, v[2]);
+        v[3] = fmaf(w[j], f[j][0].w, v[3]);
+        v[4] = fmaf(w[j], f[j][1].x, v[4]);
+        v[5] = fmaf(w[j], f[j][1].y, v[5]);
+        v[6] = fmaf(w[j], f[j][1].z, v[6]);
+        v[7] = fmaf(w[j], f[j][1].w, v[7]);
       }
     }
-    finalize_block(out_ptrs(P), v, t, h0 + hh, 32 * blk, rope);
+    finalize_eighth(out_ptrs(P), v, t, h0 + hh, 32 * blk + 8 * q, gmask, s_rope);
   }
 }
 
@@ -1533,6 +1543,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
     // every split of the (token, half) has stored its partial (the splits are
     // co-resident: this path is a cooperative launch); bounded wait on the arrival count
     const int t = c.misc[M_TOKEN], half = c.misc[M_HALF];
+    if (tid >= 32 && tid < 64) {
+      // the token's rotary table for the combine (the item buffers are gone), while the
+      // other splits are still arriving
+      float2* s_rope = reinterpret_cast<float2*>(c.sm + SM_CW) + (MAX_SPLITS * HH + HH) / 2;
+      s_rope[tid - 32] = rope_entry_of(P, t, tid - 32);
+    }
     if (tid == 0) {
       const volatile uint32_t* cnt = P.counters + (size_t)t * P.n_halves + half;
       const unsigned long long start = clock64();
