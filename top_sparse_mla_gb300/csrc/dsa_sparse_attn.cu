@@ -24,12 +24,13 @@
 //                      memory.  The one tile is the A operand of both contractions:
 //                      K-major for QK^T (M = rows), MN-major for PV (M = dims).  Raw bytes
 //                      are loaded two chunks ahead, rows are prefetched into L2 one tile
-//                      ahead.  Between items (no splits): the MXFP8 finish of output dims
-//                      128..383 of the previous item.
+//                      ahead; one tile ahead, the rotary part of the rows' keys (into
+//                      TMEM) and their block scales (into shared memory).  Between items
+//                      (no splits): the MXFP8 finish of output dims 128..383 of the
+//                      previous item.
 //   SM   (warps 8-11)  per tile: the five partial scores (four latent blocks, rope) summed
 //                      with the row's block scales, the softmax (lazy running max, exp2),
-//                      per-warp row sums, P_b hi/lo for the four PV blocks; then the
-//                      rotary part and the block scales of the next tile's rows
+//                      per-warp row sums, P_b hi/lo for the four PV blocks
 //   EPI  (warps 12-15) 1/l and the LSE; the epilogue: (O_hi + O_lo) / l out of TMEM into
 //                      the global output (dims 0..127 and 384..511, or all of it as a
 //                      split partial)
@@ -99,7 +100,8 @@ constexpr uint32_t SM_EL = SM_LW + 1024;           // 32 fp32 1/l
 constexpr uint32_t SM_ELSE = SM_EL + 128;          // 32 fp32 LSE (log2 units)
 constexpr uint32_t SM_FLAG = SM_ELSE + 128;        // 2 groups x 2 x 4 fp32
 constexpr uint32_t SM_MISC = SM_FLAG + 64;         // misc ints
-constexpr uint32_t SM_BAR = SM_MISC + 64;          // mbarriers
+constexpr uint32_t SM_SCL = SM_MISC + 64;          // 2 x 128 rows x 4 fp32 block scales (a tile's rows)
+constexpr uint32_t SM_BAR = SM_SCL + 2 * 128 * 16; // mbarriers
 constexpr uint32_t SM_END = SM_BAR + 64 * 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -770,6 +772,53 @@ DSA_DEV void dq_load_chunk(const KParams& P, uint4 (&dst)[4], int cidx, const Dq
   }
 }
 
+// The rotary part of a tile's keys and the rows' block scales, written by the dequant
+// warps one tile ahead of their use: warp w takes the tile rows 32 (w % 4) + lane (its
+// TMEM lane quarter) and rope dims 32 (w / 4) .. + 31, bf16 -> fp16 into TMEM (the A
+// operand of the rope partial, buffer gk % 2); the warps of the first half also store
+// the rows' four block scales into shared memory (SCL buffer gk % 2) for the softmax
+// warps.  Both are announced on KRFULL.
+template <bool V41>
+DSA_DEV void dq_rope(const KParams& P, const Ctx& c, uint32_t tmem, const uint32_t* list, int tt, int nrows, int w,
+                     int lane, uint32_t gk) {
+  const int q4 = w & 3, hh = w >> 2;
+  const int r = 32 * q4 + lane;
+  const bool valid = tt * TILE + r < nrows;
+  const uint32_t e = valid ? __ldcg(list + tt * TILE + r) : NO_ROW;
+  const uint32_t kb = gk & 1;
+  float4* scl = reinterpret_cast<float4*>(c.sm + SM_SCL) + 128 * kb;
+  if constexpr (V41) {   // no separate rotary keys: the four block scales only
+    if (hh == 0) {
+      const uint4 sv = valid ? row_scales<V41>(P, e) : make_uint4(0, 0, 0, 0);
+      scl[r] = make_float4(__uint_as_float(sv.x), __uint_as_float(sv.y), __uint_as_float(sv.z), __uint_as_float(sv.w));
+    }
+    arrive_w(c, B_KRFULL + kb);
+    return;
+  }
+  const uint8_t* src = valid ? row_ptr<V41>(P, e) + D_LAT : nullptr;
+  uint4 raw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) raw[k] = valid ? ldg_nc(src + 16 + 64 * hh + 16 * k) : make_uint4(0, 0, 0, 0);
+  if (hh == 0) {
+    const uint4 sv = valid ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
+    scl[r] = make_float4(__uint_as_float(sv.x), __uint_as_float(sv.y), __uint_as_float(sv.z), __uint_as_float(sv.w));
+  }
+  uint32_t v[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[4 * k + 0] = bf16x2_to_f16x2(raw[k].x);
+    v[4 * k + 1] = bf16x2_to_f16x2(raw[k].y);
+    v[4 * k + 2] = bf16x2_to_f16x2(raw[k].z);
+    v[4 * k + 3] = bf16x2_to_f16x2(raw[k].w);
+  }
+  if (!wait_bar_w(c, B_KRFREE + kb, ((gk >> 1) & 1) ^ 1)) return;
+  tc_fence_after();
+  tmem_st16(tmem + ((uint32_t)(q4 * 32) << 16) + TM_KR + 32 * kb + 16 * hh, v);
+  tc_wait_st();
+  tc_fence_before();
+  arrive_w(c, B_KRFULL + kb);
+}
+
 template <bool V41, bool FP8Q>
 DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int lane) {
   const int sub = lane >> 3, ch = lane & 7;
@@ -814,6 +863,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       if (info[IT_T] > 0) {
         if (nq > 0 && !wait_bar_w(c, B_QFREE, (nq - 1) & 1)) return -1;
         build_q<V41, FP8Q>(qa, c, b, 32 * w + lane);
+        dq_rope<V41>(P, c, tmem, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, lane, g);
         dq_load_rows(item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], w, sub, cur);
         dq_load_chunk<V41>(P, raw[0], qk_chunk(0), cur, ch);
         dq_load_chunk<V41>(P, raw[1], qk_chunk(1), cur, ch);
@@ -895,6 +945,7 @@ DSA_DEV void dq_role(const KParams& P, const Ctx& c, uint32_t tmem, int w, int l
       }
       if (more) cur = nxt;
       ++g;
+      if (more) dq_rope<V41>(P, c, tmem, list, tt + 1, nrows, w, lane, g);
       if (tt == 0 && pend >= 0 && !do_share()) return;
     }
     if (share) {
@@ -1017,49 +1068,6 @@ DSA_DEV void mma_role(const KParams& P, const Ctx& c, uint32_t tmem) {
 }
 
 // ================================================================== SX
-// The softmax warps: two groups of four; group gq takes the item's heads 16 gq ..
-// 16 gq + 15 and each of its threads one row of the tile (TMEM lane = row).  Before a
-// tile: the rotary part of its keys (bf16 -> fp16 into TMEM, the A operand of the rope
-// partial; each group converts half of the 64 dims) and the row's four block scales,
-// read one tile ahead of their use.
-template <bool V41>
-DSA_DEV void sx_rope(const KParams& P, const Ctx& c, uint32_t tmem, uint32_t tlane, const uint32_t* list, int tt,
-                     int nrows, int r, int gq, uint32_t gk, float (&scl)[4]) {
-  const bool valid = tt * TILE + r < nrows;
-  if constexpr (V41) {   // no separate rotary keys: the four block scales only
-    const uint4 sv = valid ? row_scales<V41>(P, __ldcg(list + tt * TILE + r)) : make_uint4(0, 0, 0, 0);
-    scl[0] = __uint_as_float(sv.x);
-    scl[1] = __uint_as_float(sv.y);
-    scl[2] = __uint_as_float(sv.z);
-    scl[3] = __uint_as_float(sv.w);
-    return;
-  }
-  const uint8_t* src = valid ? row_ptr<V41>(P, __ldcg(list + tt * TILE + r)) + D_LAT : nullptr;
-  uint4 raw[5];
-  raw[0] = valid ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) raw[k + 1] = valid ? ldg_nc(src + 16 + 64 * gq + 16 * k) : make_uint4(0, 0, 0, 0);
-  scl[0] = __uint_as_float(raw[0].x);
-  scl[1] = __uint_as_float(raw[0].y);
-  scl[2] = __uint_as_float(raw[0].z);
-  scl[3] = __uint_as_float(raw[0].w);
-  uint32_t v[16];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    v[4 * k + 0] = bf16x2_to_f16x2(raw[k + 1].x);
-    v[4 * k + 1] = bf16x2_to_f16x2(raw[k + 1].y);
-    v[4 * k + 2] = bf16x2_to_f16x2(raw[k + 1].z);
-    v[4 * k + 3] = bf16x2_to_f16x2(raw[k + 1].w);
-  }
-  const uint32_t kb = gk & 1;
-  if (!wait_bar_w(c, B_KRFREE + kb, ((gk >> 1) & 1) ^ 1)) return;
-  tc_fence_after();
-  tmem_st16(tmem + tlane + TM_KR + 32 * kb + 16 * gq, v);
-  tc_wait_st();
-  tc_fence_before();
-  arrive_w(c, B_KRFULL + kb);
-}
-
 // P_b = P * scale_b / reference_b of row r for the group's 16 heads, as hi / lo fp16 into
 // the row of the MN-major B operand at `base` (16-byte chunks 2 gq, 2 gq + 1: hi of the
 // group's heads; chunks 4 + 2 gq, 5 + 2 gq: their lo).
@@ -1094,7 +1102,6 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
   Group grp{B_SXG + gq, 0};     // the four warps of this group
   Group all{B_SXA, 0};          // both groups
   uint32_t g = 0, seq = 0, nq = 0, np = 0;   // tiles, items, items with tiles, partial scores
-  float scl[4] = {0.f, 0.f, 0.f, 0.f};       // block scales of row r of the next tile
   // A split of a (token, half) has stored its partial (or its LSE of -inf): it counts
   // in, and after the CTA's roles have finished every split combines one slice of it
   // (one item per CTA on this path).
@@ -1117,10 +1124,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
       if (!wait_bar_w(c, B_ITFULL + b, (seq / NB) & 1)) return -1;
       const int* info = item_info(c, b);
       if (info[IT_ITEM] < 0) return 0;
-      if (info[IT_T] > 0) {
-        sx_rope<V41>(P, c, tmem, tlane, item_list(P, b) + info[IT_ROW0], 0, info[IT_NROWS], r, gq, g, scl);
-        return c.misc[M_ABORT] ? -1 : 1;
-      }
+      if (info[IT_T] > 0) return 1;
       if (is_split) {
         // a split without a valid column: LSE -inf, so the combine gives it no weight
         // (on the queue path such items never reach this role: the prep warp writes them)
@@ -1165,7 +1169,10 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
       const bool valid = r < nrows - tt * TILE;
-      const float sc[4] = {scl[0], scl[1], scl[2], scl[3]};
+      // this row's four block scales (written with the tile's rotary keys)
+      if (!wait_bar_w(c, B_KRFULL + (g & 1), (g >> 1) & 1)) return;
+      const float4 s4 = reinterpret_cast<const float4*>(c.sm + SM_SCL)[128 * (g & 1) + r];
+      const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
       // ---- the five partial scores of row r, summed with the block scales
       float y[16];
 #pragma unroll
@@ -1272,11 +1279,7 @@ DSA_DEV void sx_role(const KParams& P, const Ctx& c, uint32_t tmem, int gq, int 
         }
       }
       ++g;
-      if (tt + 1 < T) {
-        sx_rope<V41>(P, c, tmem, tlane, list, tt + 1, nrows, r, gq, g, scl);
-        if (c.misc[M_ABORT]) return;
-        continue;
-      }
+      if (tt + 1 < T) continue;
       // ---- the item's last tile: 1/l, LSE and the epilogue of this group's heads
       if ((lane & 1) == 0) s_lw[(nq & 1) * 128 + (4 * gq + q4) * 16 + (lane >> 1)] = lw;
       if (!grp.sync(c)) return;
@@ -1484,7 +1487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) dsa_fwd_kernel(const __grid_const
       mbar_init(bar(c, B_SFREE + i), WG_SX);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(c, B_KRFULL + i), WG_SX);
+      mbar_init(bar(c, B_KRFULL + i), WG_DQ);
       mbar_init(bar(c, B_KRFREE + i), 1);
     }
     for (int i = 0; i < NB; ++i) {
