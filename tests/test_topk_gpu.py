@@ -95,3 +95,15 @@ def test_output_feeds_the_attention_indices():
     assert list(l) == [128, 100, 0]
     for t in range(3):
         assert np.all(np.diff(i[t, :l[t]]) > 0) and np.all(i[t, l[t]:] == -1)
+
+
+def test_many_rows_ragged():
+    # more rows than the GPU holds CTAs at once: ragged lengths, rows with at most k
+    # candidates and empty rows mixed in, and a row pitch of n + 8
+    rng = np.random.default_rng(25)
+    s_q, n, k = 1500, 2048, 256
+    x = _tied(rng, s_q, n, step=0.25)
+    lengths = rng.integers(-5, n + 100, size=s_q)
+    lengths[::7] = rng.integers(0, k + 1, size=len(lengths[::7]))
+    _check(x, k, lengths=list(lengths), pad=8)
+    _check(x, k)
