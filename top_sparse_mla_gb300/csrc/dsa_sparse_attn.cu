@@ -28,12 +28,13 @@
 //                      TMEM) and their block scales (into shared memory).  Between items
 //                      (no splits): the MXFP8 finish of output dims 128..383 of the
 //                      previous item.
-//   SM   (warps 8-11)  per tile: the five partial scores (four latent blocks, rope) summed
-//                      with the row's block scales, the softmax (lazy running max, exp2),
-//                      per-warp row sums, P_b hi/lo for the four PV blocks
-//   EPI  (warps 12-15) 1/l and the LSE; the epilogue: (O_hi + O_lo) / l out of TMEM into
-//                      the global output (dims 0..127 and 384..511, or all of it as a
-//                      split partial)
+//   SX   (warps 8-15)  two groups of four, 16 heads each; one thread per tile row (TMEM
+//                      lane).  Per tile: the five partial scores (four latent blocks,
+//                      rope) summed with the row's block scales, the softmax (lazy running
+//                      max, exp2), per-warp row sums, P_b hi/lo for the four PV blocks.
+//                      Last tile of an item: 1/l and the LSE, then the epilogue of output
+//                      dims 0..127 and 384..511, (O_hi + O_lo) / l out of TMEM (all 512
+//                      dims as an fp32 partial on the split path)
 //   MMA  (warp 16)     T_b[128 rows x 64] = codes_b . q~_b^T for b = 0..3 and the rope
 //                      part; O^T_b[128 dims x 64] += codes_b^T . P_b
 //   PREP (warp 17)     take an item, compact its valid index columns into a row list,
