@@ -456,7 +456,10 @@ def run_native(args):
                                    "fp16 hi + lo pairs, fp32 accumulate, MXFP8 out",
                        "timed_wall_s": wall},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": args.traffic if args.traffic is not None else profiled_traffic(args.workload),
+                         # the committed profile is of one launch of the whole workload: a token
+                         # slice (N > 1) moves other bytes
+                         "traffic": args.traffic if args.traffic is not None else
+                         (profiled_traffic(args.workload) if world == 1 or args.replicas else None),
                          "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
                                            "(profiles/dsa_fwd_kernel_decode1024_full.md)",
                          "peak_source": peak_kind,
