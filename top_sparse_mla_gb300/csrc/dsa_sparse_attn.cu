@@ -72,7 +72,7 @@ constexpr int NQ = 64;              // N of both contractions: 32 heads hi, then
 constexpr int W_SX = 8, W_MMA = 16, W_PREP = 17;
 constexpr int NWARPS = 18;
 constexpr int NTHREADS = 32 * NWARPS;
-constexpr int N_DQ = 256, N_SX = 256, N_PREP = 32;
+constexpr int N_DQ = 256, N_SX = 256;
 constexpr int WG_DQ = N_DQ / 32, WG_SX = N_SX / 32;   // warps: the unit of the handoff barriers' counts
 constexpr int MAX_SPLITS = 16;
 constexpr int NB = 4;              // item buffers: the prep warp runs up to NB - 1 items ahead
