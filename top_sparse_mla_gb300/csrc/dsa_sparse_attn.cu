@@ -787,6 +787,11 @@ DSA_DEV void dq_rope(const KParams& P, const Ctx& c, uint32_t tmem, const uint32
   const bool valid = tt * TILE + r < nrows;
   const uint32_t e = valid ? __ldcg(list + tt * TILE + r) : NO_ROW;
   const uint32_t kb = gk & 1;
+  // The scale table kb was last read by the softmax warps at the start of tile gk - 2.
+  // These warps come here for tile gk only after converting every chunk of tile gk - 1,
+  // and that waited for PV of tile gk - 2, which needs P of that tile from the softmax
+  // warps, long after their read.  So the table is written without a wait (the rotary
+  // keys' TMEM buffer, read by the tensor core, still waits for KRFREE below).
   float4* scl = reinterpret_cast<float4*>(c.sm + SM_SCL) + 128 * kb;
   if constexpr (V41) {   // no separate rotary keys: the four block scales only
     if (hh == 0) {
